@@ -1,0 +1,197 @@
+/*
+ * ck_decode.h -- C ABI of the GB300 (sm_103a) single-token attention decode
+ * step of an LLM layer with Q5_0 / Q8_0 quantized weights.
+ *
+ * The operation is the serial kernel of the page
+ * "mega_fused_attention_decode_q5_0.c" (C-Kernel-Engine): RMSNorm, Q8_0
+ * quantization of the normed activation, Q and K projections with Q5_0
+ * weights and the V projection with Q8_0 weights (each plus a bias), RoPE,
+ * the KV-cache store, GQA decode attention over the cache, Q8_0
+ * quantization of the attention output, the Q5_0 O projection with bias,
+ * and the residual add.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is a DEVICE pointer (memory of the current CUDA
+ *    device) unless stated otherwise, owned by the caller, and must be
+ *    16-byte aligned.  The library allocates nothing and keeps no pointer
+ *    after a call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is
+ *    enqueued asynchronously; no call synchronizes the stream or the device,
+ *    so every call may be recorded into a CUDA graph by stream capture.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    call that returns an error has enqueued nothing.  CK_ECUDA reports a
+ *    failed launch (cudaGetLastError after the launch).
+ *  - Weights are row-major arrays of blocks exactly as the page lays them
+ *    out: a matrix [M, K] is M rows of K/32 consecutive blocks.
+ *  - fp32 vectors are dense; KV caches are head-major fp32
+ *    [num_kv_heads, cache_capacity, head_dim]; RoPE tables are fp32
+ *    [cache_capacity, head_dim/2] (row p holds cos / sin of position p).
+ */
+#ifndef CK_DECODE_H
+#define CK_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define CK_OK 0
+#define CK_EINVAL (-1)   /* null pointer, non-positive or inconsistent size   */
+#define CK_ERANGE (-2)   /* pos / kv_tokens outside the cache                 */
+#define CK_ESCRATCH (-3) /* scratch missing or smaller than the size query    */
+#define CK_EALIGN (-4)   /* a pointer is not 16-byte aligned                  */
+#define CK_ECUDA (-5)    /* a CUDA runtime call or a kernel launch failed     */
+#define CK_ETIMEOUT (-6) /* (device status only) a bounded device wait expired */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *ck_status_string(int status);
+
+/* ---- block formats (32 weights per block) ------------------------------ */
+#define CK_QK 32
+
+/* Q5_0, 22 bytes: d = fp16 scale (little-endian bits), qh = bit 4 of each of
+ * the 32 codes (bit j <-> element j), qs[j] = low nibble of element j (bits
+ * 0-3) and of element j+16 (bits 4-7).  Weight j = (code_j - 16) * d. */
+typedef struct {
+    uint16_t d;
+    uint8_t qh[4];
+    uint8_t qs[16];
+} ck_block_q5_0;
+
+/* Q8_0, 34 bytes: d = fp16 scale, qs = 32 signed codes.  Weight j = qs[j]*d.
+ * Activations are quantized to this format with d = amax/127 (fp32) stored
+ * as fp16, and code = round-half-away-from-zero(x * (1/d)). */
+typedef struct {
+    uint16_t d;
+    int8_t qs[32];
+} ck_block_q8_0;
+
+/* ---- single steps ------------------------------------------------------ */
+
+/* quantize_row_q8_0 (page: declared, used for the normed activation and the
+ * attention output).  x: fp32 [n]; y_q8: n/32 Q8_0 blocks.  n > 0, n % 32 == 0.
+ * Bit-exact: the codes and the fp16 scale follow the rule above in IEEE
+ * fp32 (correctly rounded divide and reciprocal). */
+int ck_quantize_q8_0(const float *x, void *y_q8, int n, void *stream);
+
+/* gemv_q5_0_from_fp32 after its quantize step (page: Q5_0 GEMV with inline
+ * processing): y[r] = sum_b d_w(r,b) * d_x(b) * isum(r,b) + bias[r] for
+ * r < M, with isum the exact int32 dot of the 32 codes of block b.
+ * W: [M, K] Q5_0; x_q8: K/32 Q8_0 blocks; bias: fp32 [M] or NULL; y: fp32 [M].
+ * K % 32 == 0, M > 0. */
+int ck_gemv_q5_0_q8_0(float *y, const void *W, const void *x_q8, const float *bias, int M, int K, void *stream);
+
+/* gemv_q8_0_from_fp32 after its quantize step (page: Q8_0 GEMV, used for the
+ * V projection).  Same arguments with W: [M, K] Q8_0. */
+int ck_gemv_q8_0_q8_0(float *y, const void *W, const void *x_q8, const float *bias, int M, int K, void *stream);
+
+/* apply_rope_inline (page: RoPE application).  Rotate-half RoPE in place:
+ * with half = head_dim/2 and row `pos` of the tables, element d of every
+ * head pairs with d + half: (a, b) -> (a*cos - b*sin, a*sin + b*cos).
+ * q: fp32 [num_heads * head_dim] (may be NULL when num_heads == 0);
+ * k: fp32 [num_kv_heads * head_dim] (may be NULL when num_kv_heads == 0);
+ * rope_cos / rope_sin: fp32 [cache_capacity, head_dim/2].
+ * 0 <= pos < cache_capacity (else CK_ERANGE); head_dim even. */
+int ck_rope_inplace(float *q, float *k, const float *rope_cos, const float *rope_sin, int pos, int num_heads,
+                    int num_kv_heads, int head_dim, int cache_capacity, void *stream);
+
+/* KV-cache store (page: STEP 6).  k_cache[h][pos][:] = k[h*head_dim ...],
+ * v_cache[h][pos][:] = v[...] for every KV head h.  0 <= pos < cache_capacity. */
+int ck_kv_store(float *k_cache, float *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                int cache_capacity, int head_dim, void *stream);
+
+/* attention_forward_decode_head_major_gqa_flash (page: declared, STEP 7).
+ * For query head h, KV head g = h*num_kv_heads/num_heads and the first
+ * kv_tokens rows t of that head's cache: out_h = sum_t softmax_t(q_h.k_t /
+ * sqrt(head_dim)) v_t.  q, out: fp32 [num_heads * head_dim].
+ * Requirements: num_heads % num_kv_heads == 0, num_heads/num_kv_heads <= 8,
+ * head_dim in {32, 64, 96, 128, 256},
+ * 1 <= kv_tokens <= cache_capacity (else CK_ERANGE).
+ * `scratch` (device, >= ck_attn_scratch_size(...) bytes for a max_kv_tokens
+ * >= kv_tokens) holds the split-KV partial results; its contents need no
+ * initialization and are dead after the stream reaches the end of the call. */
+size_t ck_attn_scratch_size(int num_heads, int num_kv_heads, int max_kv_tokens, int head_dim);
+int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int num_heads,
+                       int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
+                       size_t scratch_bytes, void *stream);
+
+/* ---- the whole layer step ---------------------------------------------- */
+
+/* mega_fused_attention_decode_q5_0 (page: MAIN KERNEL).  One token at
+ * position `pos`:
+ *   out = residual + bo + Wo . q8(attention(rope(Wq.q8(rms(x))+bq),
+ *                                          cache with k, v stored at pos))
+ * x, residual, out: fp32 [embed_dim] (residual may alias x; out may not
+ * alias x, residual, weights, caches or scratch);
+ * wq: Q5_0 [num_heads*head_dim, embed_dim]; wk: Q5_0 [num_kv_heads*head_dim,
+ * embed_dim]; wv: Q8_0 [num_kv_heads*head_dim, embed_dim]; wo: Q5_0
+ * [embed_dim, num_heads*head_dim]; gamma: fp32 [embed_dim]; bq, bk, bv, bo:
+ * fp32 biases of the matching lengths, each may be NULL (= zero);
+ * k_cache, v_cache: the head-major caches, row `pos` is overwritten and rows
+ * 0..pos are attended; rope_cos / rope_sin: tables as above; eps: RMSNorm
+ * epsilon.  Requirements: embed_dim % 32 == 0, the attention requirements
+ * above, 0 <= pos < cache_capacity.
+ * `scratch`: >= ck_decode_layer_scratch_size(...) bytes of device memory
+ * (contents need no initialization).  The size depends on the current
+ * device (its SM count). */
+size_t ck_decode_layer_scratch_size(int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                    int cache_capacity);
+int ck_decode_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                    const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                    const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                    const float *rope_sin, int pos, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                    int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream);
+
+/* The same step with the position read on the device from *d_pos (int32,
+ * device memory), so that a captured CUDA graph can be replayed for
+ * successive tokens by updating *d_pos alone.  The host cannot see the
+ * position: the kernels check 0 <= *d_pos < cache_capacity themselves and,
+ * when it fails, skip all work (nothing is written) and raise CK_ERANGE in
+ * the device status word (see ck_device_status). */
+int ck_decode_layer_devpos(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                           const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                           const float *bv, const float *bo, float *k_cache, float *v_cache,
+                           const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int embed_dim,
+                           int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps,
+                           void *scratch, size_t scratch_bytes, void *stream);
+
+/* Errors that only the device can see -- a device-side position out of
+ * range (CK_ERANGE) or a bounded wait inside a kernel that expired
+ * (CK_ETIMEOUT) -- are OR-ed into one status word per device.  This call
+ * stores the most severe of them since the last call (CK_OK if none) in
+ * *status (host pointer) and clears the word.  It synchronizes `stream`:
+ * call it outside stream capture. */
+int ck_device_status(int *status, void *stream);
+
+/* Byte offset, inside a layer scratch buffer laid out for these shapes, of
+ * one intermediate that the last ck_decode_layer* call left there (valid
+ * until the next call on the same scratch):
+ *   CK_TAP_Q    fp32 [num_heads*head_dim]   q after bias and RoPE
+ *   CK_TAP_XQ8  Q8_0 [embed_dim/32]         the quantized normed input
+ *   CK_TAP_ATTN fp32 [num_heads*head_dim]   the attention output
+ *   CK_TAP_AQ8  Q8_0 [num_heads*head_dim/32] its quantization (O-proj input)
+ * Returns (size_t)-1 for an unknown tap or invalid shapes. */
+#define CK_TAP_Q 0
+#define CK_TAP_XQ8 1
+#define CK_TAP_ATTN 2
+#define CK_TAP_AQ8 3
+size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                      int cache_capacity);
+
+/* ---- test access to the integer block dots ----------------------------- */
+
+/* The per-block int32 dots that the GEMVs above compute, with the same
+ * device code: isum[r*(K/32) + b] = sum_j code_w(r,b,j) * code_x(b,j)
+ * (Q5_0 codes offset by -16).  isum: int32 [M, K/32] (device). */
+int ck_block_dots_q5_0_q8_0(int32_t *isum, const void *W, const void *x_q8, int M, int K, void *stream);
+int ck_block_dots_q8_0_q8_0(int32_t *isum, const void *W, const void *x_q8, int M, int K, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CK_DECODE_H */

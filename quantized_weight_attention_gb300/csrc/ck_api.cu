@@ -1,0 +1,404 @@
+// C ABI of libck_decode (declared in include/ck_decode.h): argument
+// validation on the host, launch planning, and the composition of the
+// decode step of the page "mega_fused_attention_decode_q5_0.c" as four
+// kernels on one stream:
+//
+//   k_qkv          RMSNorm + Q8_0 quant (prologue), Q|K|V GEMV, bias, RoPE,
+//                  KV-cache store, q                                 STEP 1-6
+//   k_attn_split   split-KV GQA-packed flash decoding                STEP 7
+//   k_attn_combine LSE merge + Q8_0 quant of the attention output    STEP 7-8
+//   k_oproj        O GEMV + bias + residual                          STEP 8
+//
+// Each kernel after the first is launched with programmatic dependent
+// launch: it starts while its predecessor drains, streams the operands that
+// do not depend on it (weights, cache rows before `pos`), then waits.
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "../../include/ck_decode.h"
+#include "ck_device.cuh"
+#include "ck_internal.h"
+
+namespace ck {
+
+__device__ unsigned g_status_word;
+
+static std::mutex g_mu;
+
+const DeviceInfo &device_info() {
+    static DeviceInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!have[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        d.smem_optin = static_cast<size_t>(optin);
+        if (d.num_sms <= 0) d.num_sms = 1;
+        cache[dev] = d;
+        have[dev] = true;
+    }
+    return cache[dev];
+}
+
+unsigned *status_word() {
+    static unsigned *cache[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned *>(p);
+    }
+    return cache[dev];
+}
+
+void ensure_smem(const void *fn, size_t bytes) {
+    static std::map<std::pair<const void *, int>, size_t> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    size_t &have = done[{fn, dev}];
+    if (have >= bytes && have != 0) return;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    have = bytes;
+}
+
+cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void **args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace ck
+
+using namespace ck;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_ptrs(std::initializer_list<const void *> required, std::initializer_list<const void *> optional) {
+    for (const void *p : required) {
+        if (!p) return CK_EINVAL;
+        if (!aligned16(p)) return CK_EALIGN;
+    }
+    for (const void *p : optional)
+        if (p && !aligned16(p)) return CK_EALIGN;
+    return CK_OK;
+}
+
+int attn_shape_ok(int H, int KV, int hd) {
+    if (H <= 0 || KV <= 0 || H % KV != 0) return CK_EINVAL;
+    if (H / KV > 8) return CK_EINVAL;
+    if (hd % 32 != 0 || hd < 32 || hd > 256) return CK_EINVAL;
+    const int dpl = hd / 32;
+    if (dpl != 1 && dpl != 2 && dpl != 3 && dpl != 4 && dpl != 8) return CK_EINVAL;
+    return CK_OK;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// Layout of the layer scratch (all offsets 256-byte aligned).
+struct LayerScratch {
+    size_t off_q, off_xq8, off_attn, off_aq8, off_part, total;
+    int splits;
+};
+
+size_t a256(size_t v) { return (v + 255) / 256 * 256; }
+
+LayerScratch layer_scratch(int D, int H, int KV, int hd, int C) {
+    LayerScratch L{};
+    L.splits = attn_splits(1, KV, C);
+    size_t o = 0;
+    L.off_q = o;
+    o = a256(o + static_cast<size_t>(H) * hd * 4);
+    L.off_xq8 = o;
+    o = a256(o + static_cast<size_t>(D / 32) * 34);
+    L.off_attn = o;
+    o = a256(o + static_cast<size_t>(H) * hd * 4);
+    L.off_aq8 = o;
+    o = a256(o + static_cast<size_t>(H * hd / 32) * 34);
+    L.off_part = o;
+    o = a256(o + attn_part_bytes(1, H, KV, hd, L.splits));
+    L.total = o;
+    return L;
+}
+
+int layer_common(float *out, const float *x, const float *residual, const void *wq, const void *wk, const void *wv,
+                 const void *wo, const float *gamma, const float *bq, const float *bk, const float *bv,
+                 const float *bo, float *k_cache, float *v_cache, const float *rope_cos, const float *rope_sin,
+                 int pos, const int32_t *d_pos, int D, int H, int KV, int hd, int C, float eps, void *scratch,
+                 size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_cache, v_cache, rope_cos, rope_sin},
+                        {bq, bk, bv, bo, d_pos});
+    if (rc) return rc;
+    if (D <= 0 || D % 32 != 0 || C <= 0) return CK_EINVAL;
+    if ((rc = attn_shape_ok(H, KV, hd))) return rc;
+    if (!d_pos && (pos < 0 || pos >= C)) return CK_ERANGE;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    const LayerScratch L = layer_scratch(D, H, KV, hd, C);
+    if (scratch_bytes < L.total) return CK_ESCRATCH;
+    if (out == x || out == residual) return CK_EINVAL;
+    uint8_t *sc = static_cast<uint8_t *>(scratch);
+    cudaStream_t s = as_stream(stream);
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
+
+    QkvArgs qa{};
+    qa.x = x;
+    qa.gamma = gamma;
+    qa.wq = static_cast<const uint8_t *>(wq);
+    qa.wk = static_cast<const uint8_t *>(wk);
+    qa.wv = static_cast<const uint8_t *>(wv);
+    qa.bq = bq;
+    qa.bk = bk;
+    qa.bv = bv;
+    qa.k_cache = k_cache;
+    qa.v_cache = v_cache;
+    qa.rope_cos = rope_cos;
+    qa.rope_sin = rope_sin;
+    qa.q_out = reinterpret_cast<float *>(sc + L.off_q);
+    qa.xq8_out = sc + L.off_xq8;
+    qa.d_pos = d_pos;
+    qa.pos = pos;
+    qa.D = D;
+    qa.H = H;
+    qa.KV = KV;
+    qa.hd = hd;
+    qa.C = C;
+    qa.eps = eps;
+    qa.status = st;
+    plan_qkv(qa);
+    if ((rc = launch_qkv(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
+
+    AttnArgs aa{};
+    aa.q = qa.q_out;
+    aa.k_cache = k_cache;
+    aa.v_cache = v_cache;
+    aa.d_pos = d_pos;
+    aa.kv_tokens = pos + 1;
+    aa.H = H;
+    aa.KV = KV;
+    aa.hd = hd;
+    aa.C = C;
+    aa.splits = L.splits;
+    aa.part = reinterpret_cast<float *>(sc + L.off_part);
+    aa.out = reinterpret_cast<float *>(sc + L.off_attn);
+    aa.out_q8 = sc + L.off_aq8;
+    aa.l2_prefetch = wo;
+    aa.l2_prefetch_bytes = static_cast<size_t>(D) * (H * hd / 32) * 22;
+    aa.status = st;
+    if (launch_attention(aa, 1, s, true, true)) return CK_ECUDA;
+
+    OprojArgs oa{};
+    oa.out = out;
+    oa.residual = residual;
+    oa.wo = static_cast<const uint8_t *>(wo);
+    oa.bo = bo;
+    oa.aq8 = sc + L.off_aq8;
+    oa.d_pos = d_pos;
+    oa.D = D;
+    oa.QD = H * hd;
+    oa.C = C;
+    oa.status = st;
+    if (launch_oproj(oa, s, true)) return CK_ECUDA;
+    return CK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ck_status_string(int status) {
+    switch (status) {
+        case CK_OK: return "CK_OK";
+        case CK_EINVAL: return "CK_EINVAL: null pointer or invalid size";
+        case CK_ERANGE: return "CK_ERANGE: position or token count outside the cache";
+        case CK_ESCRATCH: return "CK_ESCRATCH: scratch missing or too small";
+        case CK_EALIGN: return "CK_EALIGN: pointer not 16-byte aligned";
+        case CK_ECUDA: return "CK_ECUDA: CUDA launch or runtime error";
+        case CK_ETIMEOUT: return "CK_ETIMEOUT: a bounded device wait expired";
+        default: return "unknown status";
+    }
+}
+
+int ck_quantize_q8_0(const float *x, void *y_q8, int n, void *stream) {
+    int rc = check_ptrs({x, y_q8}, {});
+    if (rc) return rc;
+    if (n <= 0 || n % 32 != 0) return CK_EINVAL;
+    return launch_quantize_q8_0(x, y_q8, n, as_stream(stream)) ? CK_ECUDA : CK_OK;
+}
+
+static int gemv_common(bool q8, float *y, const void *W, const void *x_q8, const float *bias, int M, int K,
+                       void *stream) {
+    int rc = check_ptrs({y, W, x_q8}, {bias});
+    if (rc) return rc;
+    if (M <= 0 || K <= 0 || K % 32 != 0) return CK_EINVAL;
+    if (!status_word()) return CK_ECUDA;
+    return launch_gemv(q8, y, W, x_q8, bias, M, K, as_stream(stream)) ? CK_ECUDA : CK_OK;
+}
+
+int ck_gemv_q5_0_q8_0(float *y, const void *W, const void *x_q8, const float *bias, int M, int K, void *stream) {
+    return gemv_common(false, y, W, x_q8, bias, M, K, stream);
+}
+
+int ck_gemv_q8_0_q8_0(float *y, const void *W, const void *x_q8, const float *bias, int M, int K, void *stream) {
+    return gemv_common(true, y, W, x_q8, bias, M, K, stream);
+}
+
+int ck_rope_inplace(float *q, float *k, const float *rope_cos, const float *rope_sin, int pos, int num_heads,
+                    int num_kv_heads, int head_dim, int cache_capacity, void *stream) {
+    if (num_heads < 0 || num_kv_heads < 0 || head_dim <= 0 || head_dim % 2 != 0 || cache_capacity <= 0)
+        return CK_EINVAL;
+    if ((num_heads > 0 && !q) || (num_kv_heads > 0 && !k)) return CK_EINVAL;
+    int rc = check_ptrs({rope_cos, rope_sin}, {q, k});
+    if (rc) return rc;
+    if (pos < 0 || pos >= cache_capacity) return CK_ERANGE;
+    return launch_rope(q, k, rope_cos, rope_sin, pos, num_heads, num_kv_heads, head_dim, as_stream(stream))
+               ? CK_ECUDA
+               : CK_OK;
+}
+
+int ck_kv_store(float *k_cache, float *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                int cache_capacity, int head_dim, void *stream) {
+    int rc = check_ptrs({k_cache, v_cache, k, v}, {});
+    if (rc) return rc;
+    if (num_kv_heads <= 0 || head_dim <= 0 || cache_capacity <= 0) return CK_EINVAL;
+    if (pos < 0 || pos >= cache_capacity) return CK_ERANGE;
+    return launch_kv_store(k_cache, v_cache, k, v, pos, num_kv_heads, cache_capacity, head_dim, as_stream(stream))
+               ? CK_ECUDA
+               : CK_OK;
+}
+
+size_t ck_attn_scratch_size(int num_heads, int num_kv_heads, int max_kv_tokens, int head_dim) {
+    if (attn_shape_ok(num_heads, num_kv_heads, head_dim) || max_kv_tokens <= 0) return 0;
+    const int S = attn_splits(1, num_kv_heads, max_kv_tokens);
+    return attn_part_bytes(1, num_heads, num_kv_heads, head_dim, S) + 256;
+}
+
+int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int num_heads,
+                       int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
+                       size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({q, k_cache, v_cache, out}, {});
+    if (rc) return rc;
+    if ((rc = attn_shape_ok(num_heads, num_kv_heads, head_dim))) return rc;
+    if (cache_capacity <= 0) return CK_EINVAL;
+    if (kv_tokens < 1 || kv_tokens > cache_capacity) return CK_ERANGE;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    // the split count follows the token count actually attended
+    const int S = attn_splits(1, num_kv_heads, kv_tokens);
+    if (scratch_bytes < attn_part_bytes(1, num_heads, num_kv_heads, head_dim, S)) return CK_ESCRATCH;
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
+    AttnArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.kv_tokens = kv_tokens;
+    a.H = num_heads;
+    a.KV = num_kv_heads;
+    a.hd = head_dim;
+    a.C = cache_capacity;
+    a.splits = S;
+    a.part = static_cast<float *>(scratch);
+    a.out = out;
+    a.status = st;
+    return launch_attention(a, 1, as_stream(stream), false, false) ? CK_ECUDA : CK_OK;
+}
+
+size_t ck_decode_layer_scratch_size(int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                    int cache_capacity) {
+    if (embed_dim <= 0 || embed_dim % 32 || cache_capacity <= 0) return 0;
+    if (attn_shape_ok(num_heads, num_kv_heads, head_dim)) return 0;
+    return layer_scratch(embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity).total;
+}
+
+int ck_decode_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                    const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                    const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                    const float *rope_sin, int pos, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                    int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream) {
+    return layer_common(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
+                        rope_sin, pos, nullptr, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps,
+                        scratch, scratch_bytes, stream);
+}
+
+int ck_decode_layer_devpos(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                           const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                           const float *bv, const float *bo, float *k_cache, float *v_cache,
+                           const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int embed_dim,
+                           int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps,
+                           void *scratch, size_t scratch_bytes, void *stream) {
+    if (!d_pos) return CK_EINVAL;
+    return layer_common(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
+                        rope_sin, 0, d_pos, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps,
+                        scratch, scratch_bytes, stream);
+}
+
+size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                      int cache_capacity) {
+    if (ck_decode_layer_scratch_size(embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity) == 0)
+        return static_cast<size_t>(-1);
+    const LayerScratch L = layer_scratch(embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
+    switch (tap) {
+        case CK_TAP_Q: return L.off_q;
+        case CK_TAP_XQ8: return L.off_xq8;
+        case CK_TAP_ATTN: return L.off_attn;
+        case CK_TAP_AQ8: return L.off_aq8;
+        default: return static_cast<size_t>(-1);
+    }
+}
+
+int ck_device_status(int *status, void *stream) {
+    if (!status) return CK_EINVAL;
+    unsigned *w = status_word();
+    if (!w) return CK_ECUDA;
+    cudaStream_t s = as_stream(stream);
+    unsigned flags = 0;
+    if (cudaMemcpyAsync(&flags, w, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess) return CK_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CK_ECUDA;
+    if (cudaMemsetAsync(w, 0, sizeof(unsigned), s) != cudaSuccess) return CK_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CK_ECUDA;
+    *status = (flags & FLAG_TIMEOUT) ? CK_ETIMEOUT : ((flags & FLAG_RANGE) ? CK_ERANGE : CK_OK);
+    return CK_OK;
+}
+
+int ck_block_dots_q5_0_q8_0(int32_t *isum, const void *W, const void *x_q8, int M, int K, void *stream) {
+    int rc = check_ptrs({isum, W, x_q8}, {});
+    if (rc) return rc;
+    if (M <= 0 || K <= 0 || K % 32 != 0) return CK_EINVAL;
+    return launch_block_dots(false, isum, W, x_q8, M, K, as_stream(stream)) ? CK_ECUDA : CK_OK;
+}
+
+int ck_block_dots_q8_0_q8_0(int32_t *isum, const void *W, const void *x_q8, int M, int K, void *stream) {
+    int rc = check_ptrs({isum, W, x_q8}, {});
+    if (rc) return rc;
+    if (M <= 0 || K <= 0 || K % 32 != 0) return CK_EINVAL;
+    return launch_block_dots(true, isum, W, x_q8, M, K, as_stream(stream)) ? CK_ECUDA : CK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,623 @@
+// Projection kernels of the decode step (sm_103a):
+//   - Q8_0 quantization of an fp32 vector (quantize_row_q8_0),
+//   - Q5_0 x Q8_0 and Q8_0 x Q8_0 GEMV + bias (gemv_q5_0_from_fp32 /
+//     gemv_q8_0_from_fp32 after their quantize step),
+//   - the layer's fused Q|K|V projection: RMSNorm + Q8_0 quantization in
+//     the prologue, the three GEMVs, bias + RoPE + KV-cache store in the
+//     epilogue (page "mega_fused_attention_decode_q5_0.c", STEP 1-6),
+//   - the layer's O projection with bias and residual (STEP 8).
+//
+// Weight streaming.  When a row holds a multiple of 8 blocks (K % 256 == 0)
+// every 8-block segment (176 B for Q5_0, 272 B for Q8_0) is 16-byte aligned.
+// A CTA then owns a tile of rows, copies each row into padded shared memory
+// with the bulk-copy engine at kernel start (all of the CTA's bytes in
+// flight at once, before the activation is even known), and each lane
+// decodes one whole segment from 16-byte shared loads with compile-time
+// byte offsets: lane = (row within a 16-row group, one of two segment
+// columns).  Rows of other widths take a direct path: a warp per row, a
+// lane per block, aligned 32-bit global loads that never leave the block.
+#include "ck_device.cuh"
+#include "ck_internal.h"
+
+namespace ck {
+
+// ---------------------------------------------------------------------------
+// Shared-memory plan of a projection CTA (identical on host and device)
+// ---------------------------------------------------------------------------
+struct ProjSmem {
+    size_t off_w, off_xq, off_xd, off_xs, off_part, off_rowsum, off_red, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// R: max rows per CTA; nb: blocks per row; wbytes: bytes of the staged
+// weight rows (0 on the direct path).
+__host__ __device__ inline ProjSmem proj_smem(int R, int nb, size_t wbytes) {
+    ProjSmem s;
+    size_t o = 128;  // mbarriers (up to 8)
+    s.off_w = o;
+    o = align_up(o + wbytes, 16);
+    s.off_xq = o;
+    o += static_cast<size_t>(xq_chunks(nb)) * 16;
+    s.off_xd = o;
+    o += static_cast<size_t>(nb) * 4;
+    s.off_xs = o;
+    o += static_cast<size_t>(nb) * 4;
+    o = align_up(o, 16);
+    s.off_part = o;
+    o += static_cast<size_t>(nb / 8 + 1) * R * 4;
+    s.off_rowsum = o;
+    o += static_cast<size_t>(R) * 4;
+    s.off_red = o;
+    o += 64 * 4;
+    s.total = align_up(o, 128);
+    return s;
+}
+
+__host__ __device__ inline int row_stride(int nb, bool q8) { return nb * (q8 ? Q8B : Q5B) + 16; }
+
+// ---------------------------------------------------------------------------
+// Activation prologues
+// ---------------------------------------------------------------------------
+// Q8_0 blocks already in global memory -> XRow in shared memory.
+__device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int b = warp; b < nb; b += nw) {
+        const uint8_t *p = xq8 + static_cast<size_t>(b) * Q8B;
+        const int c = static_cast<int8_t>(p[2 + lane]);
+        const int sum = warp_isum(c);
+        reinterpret_cast<int8_t *>(&x.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(c);
+        if (lane == 0) {
+            x.d[b] = half_bits_to_float(static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8));
+            x.sum[b] = sum;
+        }
+    }
+}
+
+// RMSNorm (rmsnorm_forward, T = 1) followed by Q8_0 quantization, into an
+// XRow.  sum(x^2) is carried as an unevaluated fp32 pair (two-sum plus the
+// exact FMA residual of each square), so it equals the double-precision sum
+// to ~2^-46 relative; rstd = 1/sqrt(mean + eps) is then formed in double
+// and rounded once to fp32, and y = (x * rstd) * gamma in fp32.
+__device__ void xrow_rmsnorm_q8(const float *x, const float *gamma, float eps, int D, const XRow &xr, float *red,
+                                uint8_t *xq8_out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float s = 0.0f, c = 0.0f;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
+        const float v = x[i];
+        const float p = __fmul_rn(v, v);
+        const float e = fmaf(v, v, -p);
+        float t, err;
+        two_sum(s, p, t, err);
+        s = t;
+        c = __fadd_rn(c, __fadd_rn(err, e));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, err;
+        two_sum(s, s2, t, err);
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, c2), err);
+    }
+    if (lane == 0) {
+        red[2 * warp] = s;
+        red[2 * warp + 1] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        s = lane < nw ? red[2 * lane] : 0.0f;
+        c = lane < nw ? red[2 * lane + 1] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+            float t, err;
+            two_sum(s, s2, t, err);
+            s = t;
+            c = __fadd_rn(__fadd_rn(c, c2), err);
+        }
+        if (lane == 0) {
+            const double ss = static_cast<double>(s) + static_cast<double>(c);
+            red[63] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
+        }
+    }
+    __syncthreads();
+    const float rstd = red[63];
+    const int nb = D / QK;
+    for (int b = warp; b < nb; b += nw) {
+        const int i = b * QK + lane;
+        const float y = __fmul_rn(__fmul_rn(x[i], rstd), gamma[i]);
+        uint32_t dbits;
+        float dq;
+        const int q = q8_code(y, dbits, dq);
+        const int sum = warp_isum(q);
+        reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
+        if (lane == 0) {
+            xr.d[b] = dq;
+            xr.sum[b] = sum;
+        }
+        if (xq8_out) {
+            uint8_t *o = xq8_out + static_cast<size_t>(b) * Q8B;
+            o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+            if (lane == 0) {
+                o[0] = static_cast<uint8_t>(dbits & 0xFF);
+                o[1] = static_cast<uint8_t>(dbits >> 8);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ XRow xrow_at(uint8_t *smem, const ProjSmem &L) {
+    XRow x;
+    x.q = reinterpret_cast<int4 *>(smem + L.off_xq);
+    x.d = reinterpret_cast<float *>(smem + L.off_xd);
+    x.sum = reinterpret_cast<int *>(smem + L.off_xs);
+    return x;
+}
+
+// ---------------------------------------------------------------------------
+// Tile machinery
+// ---------------------------------------------------------------------------
+// Warp 0 starts the bulk copies of the tile's rows: row i of the tile is
+// global row rowof(i); rows are grouped by 16 onto one mbarrier each.
+template <typename RowFn>
+__device__ void issue_rows(uint8_t *wsm, int rstride, const uint8_t *W, int rb, int rows, uint64_t *bars,
+                           RowFn rowof) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        if (lane == 0)
+            for (int g = 0; g * 16 < rows; ++g)
+                mbar_arrive_expect_tx(&bars[g], static_cast<uint32_t>(min(16, rows - 16 * g) * rb));
+        __syncwarp();
+        for (int i = lane; i < rows; i += 32)
+            bulk_g2s(wsm + static_cast<size_t>(i) * rstride, W + static_cast<size_t>(rowof(i)) * rb,
+                     static_cast<uint32_t>(rb), &bars[i >> 4]);
+    }
+}
+
+__device__ __forceinline__ void init_bars(uint64_t *bars, int n) {
+    if (threadIdx.x == 0) {
+        for (int g = 0; g < n; ++g) mbar_init(&bars[g], 1);
+        fence_mbar_init();
+    }
+}
+
+// Segment partial sums of the staged rows: part[k * R + i] for row i and
+// segment column k.
+template <bool Q8>
+__device__ void tile_segments(const uint8_t *wsm, int rstride, int rows, int R, int nseg, uint64_t *bars,
+                              const XRow &x, float *part, unsigned *status) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int npairs = (nseg + 1) >> 1;
+    const int ngroups = (rows + 15) >> 4;
+    for (int t = warp; t < ngroups * npairs; t += nw) {
+        const int g = t / npairs, cp = t - g * npairs;
+        const int i = (g << 4) + (lane & 15);
+        const int k = (cp << 1) + (lane >> 4);
+        if (!mbar_wait(&bars[g], 0)) flag_error(status, FLAG_TIMEOUT);
+        if (i < rows && k < nseg)
+            part[k * R + i] = seg_dot<Q8>(
+                reinterpret_cast<const uint4 *>(wsm + static_cast<size_t>(i) * rstride + k * SegShape<Q8>::BYTES),
+                x, k * 8);
+    }
+}
+
+// rowsum[i] = sum_k part[k * R + i], 8 lanes per row, fixed order.
+__device__ void reduce_rows(const float *part, int R, int rows, int nseg, float *rowsum) {
+    const int n = (rows * 8 + 31) & ~31;
+    for (int it = threadIdx.x; it < n; it += blockDim.x) {
+        const int i = it >> 3, sub = it & 7;
+        float s = 0.0f;
+        if (i < rows)
+            for (int k = sub; k < nseg; k += 8) s += part[k * R + i];
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 2);
+        s += __shfl_xor_sync(0xffffffffu, s, 1);
+        if (sub == 0 && i < rows) rowsum[i] = s;
+    }
+}
+
+// Direct path: a warp per row, a lane per block.
+template <bool Q8, typename RowFn>
+__device__ void tile_direct(const uint8_t *W, int nb, int rows, RowFn rowof, const XRow &x, float *rowsum) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    constexpr int BLK = Q8 ? Q8B : Q5B;
+    for (int i = warp; i < rows; i += nw) {
+        const size_t r = static_cast<size_t>(rowof(i));
+        float acc = 0.0f;
+        for (int b = lane; b < nb; b += 32) acc += block_dot_global<Q8>(W, (r * nb + b) * BLK, x, b);
+        acc = warp_sum(acc);
+        if (lane == 0) rowsum[i] = acc;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Standalone kernels
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quantize_q8_0(const float *__restrict__ x, uint8_t *__restrict__ y, int nb) {
+    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= nb) return;
+    const int lane = threadIdx.x & 31;
+    uint32_t dbits;
+    float dq;
+    const int q = q8_code(x[static_cast<size_t>(b) * QK + lane], dbits, dq);
+    uint8_t *o = y + static_cast<size_t>(b) * Q8B;
+    o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    if (lane == 0) {
+        o[0] = static_cast<uint8_t>(dbits & 0xFF);
+        o[1] = static_cast<uint8_t>(dbits >> 8);
+    }
+}
+
+template <bool Q8, bool FAST>
+__global__ void __launch_bounds__(512) k_gemv(float *__restrict__ y, const uint8_t *__restrict__ W,
+                                              const uint8_t *__restrict__ xq8, const float *__restrict__ bias,
+                                              int M, int K, int R, unsigned *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nb = K / QK, nseg = nb / 8;
+    const int rb = nb * (Q8 ? Q8B : Q5B);
+    const int rstride = row_stride(nb, Q8);
+    const int r0 = blockIdx.x * R;
+    const int rows = min(R, M - r0);
+    const ProjSmem L = proj_smem(R, nb, FAST ? static_cast<size_t>(R) * rstride : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *wsm = smem + L.off_w;
+    float *part = reinterpret_cast<float *>(smem + L.off_part);
+    float *rowsum = reinterpret_cast<float *>(smem + L.off_rowsum);
+    const XRow x = xrow_at(smem, L);
+    auto rowof = [r0](int i) { return r0 + i; };
+    if constexpr (FAST) {
+        init_bars(bars, (rows + 15) >> 4);
+        __syncthreads();
+        issue_rows(wsm, rstride, W, rb, rows, bars, rowof);
+    }
+    xrow_from_q8(xq8, nb, x);
+    __syncthreads();
+    if constexpr (FAST) {
+        tile_segments<Q8>(wsm, rstride, rows, R, nseg, bars, x, part, status);
+        __syncthreads();
+        reduce_rows(part, R, rows, nseg, rowsum);
+    } else {
+        tile_direct<Q8>(W, nb, rows, rowof, x, rowsum);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) y[r0 + i] = rowsum[i] + (bias ? bias[r0 + i] : 0.0f);
+}
+
+// Per-block int32 dots with the GEMV's own decode path (test access).
+template <bool Q8>
+__global__ void __launch_bounds__(256) k_block_dots(int32_t *__restrict__ isum, const uint8_t *__restrict__ W,
+                                                    const uint8_t *__restrict__ xq8, int M, int K) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nb = K / QK;
+    const ProjSmem L = proj_smem(1, nb, 0);
+    const XRow x = xrow_at(smem, L);
+    xrow_from_q8(xq8, nb, x);
+    __syncthreads();
+    constexpr int BLK = Q8 ? Q8B : Q5B;
+    if (nb % 8 == 0) {
+        const int nseg = nb / 8;
+        const long task = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (task >= static_cast<long>(M) * nseg) return;
+        const long r = task / nseg, k = task % nseg;
+        const uint4 *seg = reinterpret_cast<const uint4 *>(W + (r * nb + k * 8) * BLK);
+        int out[8];
+        seg_dot<Q8>(seg, x, static_cast<int>(k) * 8, out);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) isum[r * nb + k * 8 + j] = out[j];
+    } else {
+        const long task = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x;
+        if (task >= static_cast<long>(M) * nb) return;
+        const long r = task / nb, b = task % nb;
+        int out;
+        block_dot_global<Q8>(W, static_cast<size_t>(r * nb + b) * BLK, x, static_cast<int>(b), &out);
+        isum[r * nb + b] = out;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The layer's fused Q|K|V projection (STEP 1-6)
+// ---------------------------------------------------------------------------
+// Tiles: Q and K tiles hold 16 RoPE pairs of one head (rows h*hd + i0 + i
+// and h*hd + hd/2 + i0 + i, i < 16), so the epilogue rotates without a
+// second pass; V tiles hold rv consecutive rows.
+struct QkvTile {
+    int kind;  // 0 = Q, 1 = K, 2 = V
+    int head, i0, v0, rows;
+};
+
+__device__ __forceinline__ QkvTile qkv_tile(const QkvArgs &a, int t) {
+    QkvTile T{};
+    const int sub = a.hd >> 5;  // RoPE pair-tiles per head
+    if (t < a.n_q_tiles) {
+        T.kind = 0;
+        T.head = t / sub;
+        T.i0 = (t % sub) << 4;
+        T.rows = 32;
+    } else if (t < a.n_q_tiles + a.n_k_tiles) {
+        const int u = t - a.n_q_tiles;
+        T.kind = 1;
+        T.head = u / sub;
+        T.i0 = (u % sub) << 4;
+        T.rows = 32;
+    } else {
+        T.kind = 2;
+        T.v0 = (t - a.n_q_tiles - a.n_k_tiles) * a.rv;
+        T.rows = min(a.rv, a.KV * a.hd - T.v0);
+    }
+    return T;
+}
+
+__host__ __device__ inline size_t qkv_wbytes(int nb, int rv) {
+    const size_t a = 32u * static_cast<size_t>(row_stride(nb, false));
+    const size_t b = static_cast<size_t>(rv) * row_stride(nb, true);
+    return a > b ? a : b;
+}
+
+template <bool FAST>
+__global__ void __launch_bounds__(512, 1) k_qkv(const QkvArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const QkvTile T = qkv_tile(a, blockIdx.x);
+    const int half = a.hd >> 1;
+    const int nb = a.D / QK, nseg = nb / 8;
+    const bool q8 = T.kind == 2;
+    const uint8_t *W = T.kind == 0 ? a.wq : (T.kind == 1 ? a.wk : a.wv);
+    const int rb = nb * (q8 ? Q8B : Q5B);
+    const int rstride = row_stride(nb, q8);
+    const int Rmax = max(32, a.rv);
+    const ProjSmem L = proj_smem(Rmax, nb, FAST ? qkv_wbytes(nb, a.rv) : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *wsm = smem + L.off_w;
+    float *part = reinterpret_cast<float *>(smem + L.off_part);
+    float *rowsum = reinterpret_cast<float *>(smem + L.off_rowsum);
+    float *red = reinterpret_cast<float *>(smem + L.off_red);
+    const XRow x = xrow_at(smem, L);
+    auto rowof = [&](int i) {
+        return T.kind == 2 ? T.v0 + i : T.head * a.hd + (i < 16 ? T.i0 + i : half + T.i0 + i - 16);
+    };
+
+    const int pos = a.d_pos ? *a.d_pos : a.pos;
+    if (pos < 0 || pos >= a.C) {  // uniform over the grid: nothing is written
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
+        pdl_wait();  // completion of this grid must still imply completion of the one before
+        return;
+    }
+    if constexpr (FAST) {
+        init_bars(bars, (T.rows + 15) >> 4);
+        __syncthreads();
+        issue_rows(wsm, rstride, W, rb, T.rows, bars, rowof);  // weights do not depend on earlier grids
+    }
+    pdl_trigger();
+    pdl_wait();  // x may be the previous layer's output
+    xrow_rmsnorm_q8(a.x, a.gamma, a.eps, a.D, x, red, blockIdx.x == 0 ? a.xq8_out : nullptr);
+    __syncthreads();
+    if constexpr (FAST) {
+        if (q8)
+            tile_segments<true>(wsm, rstride, T.rows, Rmax, nseg, bars, x, part, a.status);
+        else
+            tile_segments<false>(wsm, rstride, T.rows, Rmax, nseg, bars, x, part, a.status);
+        __syncthreads();
+        reduce_rows(part, Rmax, T.rows, nseg, rowsum);
+    } else {
+        if (q8)
+            tile_direct<true>(W, nb, T.rows, rowof, x, rowsum);
+        else
+            tile_direct<false>(W, nb, T.rows, rowof, x, rowsum);
+    }
+    __syncthreads();
+
+    if (T.kind == 2) {
+        for (int i = threadIdx.x; i < T.rows; i += blockDim.x) {
+            const int r = T.v0 + i;
+            const float v = rowsum[i] + (a.bv ? a.bv[r] : 0.0f);
+            const int h = r / a.hd, d = r - h * a.hd;
+            a.v_cache[(static_cast<size_t>(h) * a.C + pos) * a.hd + d] = v;
+        }
+    } else if (threadIdx.x < 16) {
+        // bias, then rotate-half RoPE of the pair (d, d + hd/2) at row `pos`
+        const int i = threadIdx.x, d = T.i0 + i;
+        const int ra = rowof(i), rb2 = rowof(16 + i);
+        const float *bias = T.kind == 0 ? a.bq : a.bk;
+        const float A = rowsum[i] + (bias ? bias[ra] : 0.0f);
+        const float B = rowsum[16 + i] + (bias ? bias[rb2] : 0.0f);
+        const float c = a.rope_cos[static_cast<size_t>(pos) * half + d];
+        const float s = a.rope_sin[static_cast<size_t>(pos) * half + d];
+        const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, s));
+        const float B2 = __fadd_rn(__fmul_rn(A, s), __fmul_rn(B, c));
+        if (T.kind == 0) {
+            a.q_out[ra] = A2;
+            a.q_out[rb2] = B2;
+        } else {
+            float *kr = a.k_cache + (static_cast<size_t>(T.head) * a.C + pos) * a.hd;
+            kr[d] = A2;
+            kr[d + half] = B2;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The layer's O projection + bias + residual (STEP 8)
+// ---------------------------------------------------------------------------
+template <bool FAST>
+__global__ void __launch_bounds__(512, 1) k_oproj(const OprojArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int nb = a.QD / QK, nseg = nb / 8;
+    const int rb = nb * Q5B;
+    const int rstride = row_stride(nb, false);
+    const int R = a.rows_per_cta;
+    const int r0 = blockIdx.x * R;
+    const int rows = min(R, a.D - r0);
+    const ProjSmem L = proj_smem(R, nb, FAST ? static_cast<size_t>(R) * rstride : 0);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *wsm = smem + L.off_w;
+    float *part = reinterpret_cast<float *>(smem + L.off_part);
+    float *rowsum = reinterpret_cast<float *>(smem + L.off_rowsum);
+    const XRow x = xrow_at(smem, L);
+    auto rowof = [r0](int i) { return r0 + i; };
+    if (a.d_pos) {
+        const int pos = *a.d_pos;
+        if (pos < 0 || pos >= a.C) {
+            pdl_wait();
+            return;
+        }
+    }
+    if constexpr (FAST) {
+        init_bars(bars, (rows + 15) >> 4);
+        __syncthreads();
+        issue_rows(wsm, rstride, a.wo, rb, rows, bars, rowof);
+    }
+    pdl_trigger();
+    pdl_wait();  // the attention output is ready
+    xrow_from_q8(a.aq8, nb, x);
+    __syncthreads();
+    if constexpr (FAST) {
+        tile_segments<false>(wsm, rstride, rows, R, nseg, bars, x, part, a.status);
+        __syncthreads();
+        reduce_rows(part, R, rows, nseg, rowsum);
+    } else {
+        tile_direct<false>(a.wo, nb, rows, rowof, x, rowsum);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+        const int r = r0 + i;
+        const float o = rowsum[i] + (a.bo ? a.bo[r] : 0.0f);
+        a.out[r] = o + a.residual[r];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? 0 : -5; }
+
+template <typename F>
+static void set_smem(F *fn, size_t bytes) {
+    ensure_smem(reinterpret_cast<const void *>(fn), bytes);
+}
+
+int launch_quantize_q8_0(const float *x, void *y, int n, cudaStream_t s) {
+    const int nb = n / QK;
+    const int wpb = 8;
+    k_quantize_q8_0<<<(nb + wpb - 1) / wpb, 32 * wpb, 0, s>>>(x, static_cast<uint8_t *>(y), nb);
+    return cuda_status(cudaGetLastError());
+}
+
+// Rows per CTA for a standalone GEMV: about one CTA per SM, at most 64 rows
+// (4 mbarrier groups) and at most ~200 KB of staged rows.
+static int gemv_rows_per_cta(int M, int nb, bool q8) {
+    const DeviceInfo &di = device_info();
+    int R = (M + di.num_sms - 1) / di.num_sms;
+    const int rs = row_stride(nb, q8);
+    const int cap = static_cast<int>((di.smem_optin - 16384) / static_cast<size_t>(rs));
+    R = R < 1 ? 1 : R;
+    R = R > 64 ? 64 : R;
+    return R > cap ? cap : R;
+}
+
+int launch_gemv(bool q8, float *y, const void *W, const void *xq8, const float *bias, int M, int K, cudaStream_t s) {
+    const int nb = K / QK;
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    const uint8_t *x = static_cast<const uint8_t *>(xq8);
+    const bool fast = (nb % 8 == 0) && gemv_rows_per_cta(M, nb, q8) >= 1;
+    if (fast) {
+        const int R = gemv_rows_per_cta(M, nb, q8);
+        const ProjSmem L = proj_smem(R, nb, static_cast<size_t>(R) * row_stride(nb, q8));
+        const int grid = (M + R - 1) / R;
+        const int tasks = ((R + 15) / 16) * ((nb / 8 + 1) / 2);
+        const int threads = 32 * (tasks < 1 ? 1 : (tasks > 16 ? 16 : tasks));
+        if (q8) {
+            set_smem(k_gemv<true, true>, L.total);
+            k_gemv<true, true><<<grid, threads, L.total, s>>>(y, w, x, bias, M, K, R, status_word());
+        } else {
+            set_smem(k_gemv<false, true>, L.total);
+            k_gemv<false, true><<<grid, threads, L.total, s>>>(y, w, x, bias, M, K, R, status_word());
+        }
+    } else {
+        const int R = 8;
+        const ProjSmem L = proj_smem(R, nb, 0);
+        const int grid = (M + R - 1) / R;
+        if (q8) {
+            set_smem(k_gemv<true, false>, L.total);
+            k_gemv<true, false><<<grid, 256, L.total, s>>>(y, w, x, bias, M, K, R, status_word());
+        } else {
+            set_smem(k_gemv<false, false>, L.total);
+            k_gemv<false, false><<<grid, 256, L.total, s>>>(y, w, x, bias, M, K, R, status_word());
+        }
+    }
+    return cuda_status(cudaGetLastError());
+}
+
+int launch_block_dots(bool q8, int32_t *isum, const void *W, const void *xq8, int M, int K, cudaStream_t s) {
+    const int nb = K / QK;
+    const ProjSmem L = proj_smem(1, nb, 0);
+    const long tasks = (nb % 8 == 0) ? static_cast<long>(M) * (nb / 8) : static_cast<long>(M) * nb;
+    const int grid = static_cast<int>((tasks + 255) / 256);
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    const uint8_t *x = static_cast<const uint8_t *>(xq8);
+    if (q8) {
+        set_smem(k_block_dots<true>, L.total);
+        k_block_dots<true><<<grid, 256, L.total, s>>>(isum, w, x, M, K);
+    } else {
+        set_smem(k_block_dots<false>, L.total);
+        k_block_dots<false><<<grid, 256, L.total, s>>>(isum, w, x, M, K);
+    }
+    return cuda_status(cudaGetLastError());
+}
+
+void plan_qkv(QkvArgs &a) {
+    const DeviceInfo &di = device_info();
+    const int sub = a.hd / 32;
+    a.n_q_tiles = a.H * sub;
+    a.n_k_tiles = a.KV * sub;
+    const int KD = a.KV * a.hd;
+    const int rem = di.num_sms - a.n_q_tiles - a.n_k_tiles;
+    int rv = rem > 0 ? (KD + rem - 1) / rem : 32;
+    rv = rv < 8 ? 8 : (rv > 48 ? 48 : rv);
+    a.rv = rv;
+}
+
+static bool qkv_fast(const QkvArgs &a, size_t *smem_total) {
+    const int nb = a.D / QK;
+    const bool fast = nb % 8 == 0;
+    const ProjSmem L = proj_smem(a.rv > 32 ? a.rv : 32, nb, fast ? qkv_wbytes(nb, a.rv) : 0);
+    *smem_total = L.total;
+    return fast;
+}
+
+int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl) {
+    size_t smem;
+    const bool fast = qkv_fast(a, &smem);
+    if (smem > device_info().smem_optin) return -1;
+    const int nb = a.D / QK;
+    const int v_tiles = (a.KV * a.hd + a.rv - 1) / a.rv;
+    const int grid = a.n_q_tiles + a.n_k_tiles + v_tiles;
+    const int tasks = 2 * ((nb / 8 + 1) / 2);
+    const int vt = ((a.rv + 15) / 16) * ((nb / 8 + 1) / 2);
+    int warps = fast ? (tasks > vt ? tasks : vt) : 8;
+    warps = warps < 4 ? 4 : (warps > 16 ? 16 : warps);
+    QkvArgs arg = a;
+    void *args[] = {&arg};
+    const void *fn = fast ? reinterpret_cast<const void *>(k_qkv<true>) : reinterpret_cast<const void *>(k_qkv<false>);
+    ensure_smem(fn, smem);
+    return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), smem, s, pdl, args));
+}
+
+int launch_oproj(const OprojArgs &a0, cudaStream_t s, bool pdl) {
+    OprojArgs a = a0;
+    const int nb = a.QD / QK;
+    const bool fast = nb % 8 == 0;
+    a.rows_per_cta = fast ? gemv_rows_per_cta(a.D, nb, false) : 8;
+    const int R = a.rows_per_cta;
+    const ProjSmem L = proj_smem(R, nb, fast ? static_cast<size_t>(R) * row_stride(nb, false) : 0);
+    const int grid = (a.D + R - 1) / R;
+    int warps = fast ? ((R + 15) / 16) * ((nb / 8 + 1) / 2) : 8;
+    warps = warps < 4 ? 4 : (warps > 16 ? 16 : warps);
+    void *args[] = {&a};
+    const void *fn = fast ? reinterpret_cast<const void *>(k_oproj<true>) : reinterpret_cast<const void *>(k_oproj<false>);
+    ensure_smem(fn, L.total);
+    return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), L.total, s, pdl, args));
+}
+
+}  // namespace ck

@@ -1,0 +1,88 @@
+// Host-side interfaces between the translation units of libck_decode.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ck {
+
+// Per-device facts the launch planner needs (cached per device ordinal).
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    size_t smem_optin;  // max dynamic shared memory per block (opt-in)
+};
+const DeviceInfo &device_info();
+
+// Address of the library's device status word on the current device.
+unsigned *status_word();
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device (a runtime call only the first time a larger value is needed).
+void ensure_smem(const void *fn, size_t bytes);
+
+// Launch helper: optional programmatic-dependent-launch attribute.
+cudaError_t launch(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void **args);
+
+// ---- gemv / quantize (ck_gemv.cu) ----
+int launch_quantize_q8_0(const float *x, void *y, int n, cudaStream_t s);
+int launch_gemv(bool q8, float *y, const void *W, const void *xq8, const float *bias, int M, int K, cudaStream_t s);
+int launch_block_dots(bool q8, int32_t *isum, const void *W, const void *xq8, int M, int K, cudaStream_t s);
+
+// The layer's projection kernels.
+struct QkvArgs {
+    const float *x, *gamma;
+    const uint8_t *wq, *wk, *wv;
+    const float *bq, *bk, *bv;
+    float *k_cache, *v_cache;
+    const float *rope_cos, *rope_sin;
+    float *q_out;        // [H*hd] rotated q
+    uint8_t *xq8_out;    // [D/32] Q8_0 blocks of the normed input (written by CTA 0)
+    const int32_t *d_pos;  // device position (or null: use pos)
+    int pos;
+    int D, H, KV, hd, C;
+    float eps;
+    int n_q_tiles, n_k_tiles, rv;  // Q / K tiles of 16 RoPE pairs, V tiles of rv rows
+    unsigned *status;
+};
+struct OprojArgs {
+    float *out;
+    const float *residual;
+    const uint8_t *wo;
+    const float *bo;
+    const uint8_t *aq8;  // [H*hd/32] Q8_0 blocks of the attention output
+    const int32_t *d_pos;
+    int D, QD, rows_per_cta, C;
+    unsigned *status;
+};
+int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl);
+int launch_oproj(const OprojArgs &a, cudaStream_t s, bool pdl);
+void plan_qkv(QkvArgs &a);
+
+// ---- attention (ck_attn.cu) ----
+struct AttnArgs {
+    const float *q;           // [B][H*hd]
+    const float *k_cache;     // single sequence: the cache; batched: unused
+    const float *v_cache;
+    const float *const *k_caches;  // batched: device array of B cache pointers
+    const float *const *v_caches;
+    const int32_t *d_pos;     // device positions [B] (T = pos + 1) or null
+    int kv_tokens;            // used when d_pos is null (B == 1)
+    int H, KV, hd, C;
+    int splits;               // S
+    float *part;              // scratch: partial results
+    float *out;               // [B][H*hd] fp32 attention output
+    uint8_t *out_q8;          // [B][H*hd/32] Q8_0 blocks, or null
+    const void *l2_prefetch;  // optional: bytes the next kernel reads, pulled into L2
+    size_t l2_prefetch_bytes;
+    unsigned *status;
+};
+size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
+int attn_splits(int B, int KV, int max_tokens);
+int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine);
+int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, int H, int KV, int hd, cudaStream_t s);
+int launch_kv_store(float *kc, float *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
+                    cudaStream_t s);
+
+}  // namespace ck
