@@ -1,0 +1,489 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the Q5_0/Q8_0 attention layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
+
+A step is one decode step of the layer (RMSNorm -> Q8_0 -> Q/K/V GEMVs ->
+RoPE -> KV store -> GQA attention -> Q8_0 -> O GEMV + residual) for one token.
+Default workload: the 7B-class layer at 8K context (D=3584, 28/4 heads,
+head_dim 128, 8193 cache rows attended).  Inputs are seeded synthetic data.
+Each step uses the next of R byte-identical replicas of weights + caches, so
+the bytes touched between two uses of a replica exceed the 129 MB L2.
+
+Device timing: K steps replayed from CUDA graphs (R steps per graph), CUDA
+events on the replay stream, barrier + synchronize on both sides, max over
+ranks.  e2e: the same steps through the C-ABI call with the input copied from
+pinned host memory and the output read back every step.  Under torchrun each
+rank runs its own replica set ("replicas only": the decode step of one
+sequence has no data-parallel split that needs a collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode layer-steps/s (tokens/s) and achieved HBM GB/s vs GB300 peak"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=60000)
+    p.add_argument("--warmup", type=int, default=600)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="7b8k", choices=["tiny", "small1k", "7b8k", "stack32k"])
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# --------------------------------------------------------------------------
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo")
+        pg = dist
+    return ws, rank, local, pg
+
+
+def barrier(pg, torch):
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(pg, torch, v: float) -> float:
+    if pg is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id, self.rows, self.proc = gpu_id, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        ok = [r for r in self.rows if len(r) >= 8]
+        sm = [float(r[0]) for r in ok if num(r[0])]
+        mx = [float(r[1]) for r in ok if num(r[1])]
+        pw = [float(r[2]) for r in ok if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in ok for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def profiled_traffic(kernel: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the kernel source as it is now (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        src = open(os.path.join(ROOT, source), "rb").read()
+        entry = d.get(kernel)
+        if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
+            return entry.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------
+# the workload on the device
+# --------------------------------------------------------------------------
+class Source:
+    """Device copies of one seeded layer (the replicas clone it)."""
+
+    def __init__(self, torch, w, dev):
+        from quantized_weight_attention_gb300 import synth
+        L = synth.make_layer(w)
+        cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+        T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        self.t = dict(x=T(L.x), gamma=T(L.gamma), wq=T(L.wq), wk=T(L.wk), wv=T(L.wv), wo=T(L.wo), bq=T(L.bq),
+                      bk=T(L.bk), bv=T(L.bv), bo=T(L.bo), kc=T(L.k_cache), vc=T(L.v_cache), cos=T(cos), sin=T(sin))
+
+
+class Replica:
+    """An independent byte copy of one layer's weights, caches and scratch."""
+
+    def __init__(self, torch, q, src, w, dev):
+        self.w = w
+        self.t = {k: v.clone() for k, v in src.t.items()}
+        self.out = torch.empty(w.D, dtype=torch.float32, device=dev)
+        self.nbytes = q.ck_decode_layer_scratch_size(w.D, w.H, w.KV, w.hd, w.capacity)
+        self.scratch = torch.empty(self.nbytes, dtype=torch.uint8, device=dev)
+
+    def call(self, q, stream, x=None):
+        w, t = self.w, self.t
+        xx = t["x"] if x is None else x
+        return q.ck_decode_layer(self.out, xx, xx, t["wq"], t["wk"], t["wv"], t["wo"], t["gamma"], t["bq"], t["bk"],
+                                 t["bv"], t["bo"], t["kc"], t["vc"], t["cos"], t["sin"], w.pos, w.D, w.H, w.KV, w.hd,
+                                 w.capacity, w.eps, self.scratch, self.nbytes, stream)
+
+
+def step_bytes(w):
+    """Algorithmic bytes of one step: quantized weights + the K and V rows attended."""
+    return w.weight_bytes() + w.kv_read_bytes(w.pos + 1)
+
+
+def gpu_uuid(torch, dev):
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    return uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+
+
+def run_ours(args, ws, rank, local, pg):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_weight_attention_gb300 as q
+    from quantized_weight_attention_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.config]
+    if args.config == "stack32k":
+        return run_stack(args, ws, pg, torch, q, synth, dev)
+    src = Source(torch, w, dev)
+    per_replica = w.weight_bytes() + 2 * w.KV * w.capacity * w.hd * 4 + 4 * w.D * 8
+    R = max(3, -(-int(2.5 * L2_BYTES) // per_replica))
+    reps = [Replica(torch, q, src, w, dev) for _ in range(R)]
+    del src
+    stream = torch.cuda.Stream(device=dev)
+    for r in reps:  # eager first calls (kernel attributes are set outside capture), checked
+        q.check(r.call(q, stream.cuda_stream))
+    torch.cuda.synchronize()
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                q.check(reps[i % R].call(q, stream.cuda_stream))
+        return g
+
+    g_full = capture(R)
+    K, W = args.steps, max(args.warmup, 3)
+    rem = K % R
+    g_rem = capture(rem) if rem else None
+    for _ in range(-(-W // R)):
+        g_full.replay()
+    W = -(-W // R) * R
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(K // R):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    value = ws * K / sec
+
+    # ---- dominant kernel: the attention over the cache, launched back to
+    # back behind a sleeping kernel so that CPU launch gaps do not enter
+    att_bytes = w.kv_read_bytes(w.pos + 1)
+    att_scr = q.ck_attn_scratch_size(w.H, w.KV, w.capacity, w.hd)
+    att_scratch = torch.empty(att_scr, dtype=torch.uint8, device=dev)
+    att_out = torch.empty(w.H * w.hd, dtype=torch.float32, device=dev)
+    qoff = q.ck_decode_layer_scratch_offset(q.CK_TAP_Q, w.D, w.H, w.KV, w.hd, w.capacity)
+    qtap = [r.scratch[qoff:qoff + w.H * w.hd * 4].view(torch.float32) for r in reps]
+    durs = []
+    with torch.cuda.stream(stream):
+        for rnd in range(6):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2 * R)]
+            torch.cuda._sleep(4_000_000)
+            for i, (a, b) in enumerate(evs):
+                r = reps[i % R]
+                a.record(stream)
+                q.check(q.ck_attn_decode_gqa(qtap[i % R], r.t["kc"], r.t["vc"], att_out, w.H, w.KV, w.pos + 1,
+                                             w.capacity, w.hd, att_scratch, att_scr, stream.cuda_stream))
+                b.record(stream)
+            stream.synchronize()
+            if rnd:  # the first round warms up
+                durs += [a.elapsed_time(b) for a, b in evs]
+    att_ms = statistics.median(durs)
+    peak, peak_kind = measured_peaks()
+    achieved = att_bytes / (att_ms / 1e3) / 1e9
+
+    # ---- e2e through the C ABI with host buffers
+    Ke = min(K, 20000)
+    xh = reps[0].t["x"].cpu().pin_memory()
+    outh = torch.empty((R, w.D), dtype=torch.float32).pin_memory()
+    xdev = [torch.empty(w.D, dtype=torch.float32, device=dev) for _ in range(R)]
+    torch.cuda.synchronize()
+    barrier(pg, torch)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(Ke):
+            j = i % R
+            xdev[j].copy_(xh, non_blocking=True)
+            q.check(reps[j].call(q, stream.cuda_stream, x=xdev[j]))
+            outh[j].copy_(reps[j].out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    barrier(pg, torch)
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1))
+    e2e_value = ws * Ke / (e2e_ms / 1e3)
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "layer-steps/s", "n_gpus": ws, "steps": K, "warmup": W,
+        "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 dot (dp4a) + fp32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: one decode step of a D={w.D}, {w.H}/{w.KV}-head, head_dim {w.hd} layer "
+                               f"at pos {w.pos} ({w.pos + 1} cache rows attended, capacity {w.capacity}); "
+                               f"Q5_0 Wq/Wk/Wo, Q8_0 Wv, fp32 head-major KV cache",
+                   "l2": f"inputs larger than L2: {R} replicas of weights+caches rotated, "
+                         f"{R * per_replica / 2**20:.0f} MiB touched between reuses",
+                   "graph_steps": R, "parallelism": f"replicas x{ws}"},
+        "step_hbm_gbs": round(step_bytes(w) * ws * K / sec / 1e9, 1),
+        "step_bytes": step_bytes(w),
+        "roofline": {"kernel": "attention (k_attn_split + k_attn_combine, one C-ABI call)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": att_bytes, "ms_per_launch": round(att_ms, 6),
+                     "traffic": profiled_traffic("k_attn_split",
+                                                 "quantized_weight_attention_gb300/csrc/ck_attn.cu")},
+        "e2e": {"value": round(e2e_value, 1), "unit": "layer-steps/s", "h2d_bytes_per_step": w.D * 4,
+                "d2h_bytes_per_step": w.D * 4, "steps": Ke,
+                "how": "per step: pinned x -> device, ck_decode_layer, out -> pinned host (one stream)"},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+def run_stack(args, ws, pg, torch, q, synth, dev):
+    """28 layers of the 7B shape at 32K context: one token through the stack per step."""
+    w = synth.WORKLOADS["stack32k"]
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    gen = torch.Generator(device=dev)
+    layers = []
+    for layer in range(w.layers):
+        gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
+        gen.manual_seed(w.seed * 1000 + layer)
+        kc = torch.zeros((w.KV, w.capacity, w.hd), dtype=torch.float32, device=dev)
+        vc = torch.zeros_like(kc)
+        kc[:, :w.pos].normal_(generator=gen)
+        vc[:, :w.pos].normal_(generator=gen)
+        layers.append(dict(gamma=T(gamma), wq=T(wq), wk=T(wk), wv=T(wv), wo=T(wo), bq=T(bq), bk=T(bk), bv=T(bv),
+                           bo=T(bo), kc=kc, vc=vc))
+    cosd, sind = T(cos), T(sin)
+    x0 = T(rng.standard_normal(w.D).astype(np.float32))
+    bufs = [torch.empty(w.D, dtype=torch.float32, device=dev) for _ in range(2)]
+    nbytes = q.ck_decode_layer_scratch_size(w.D, w.H, w.KV, w.hd, w.capacity)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def token():
+        x = x0
+        for i, Lr in enumerate(layers):
+            out = bufs[i % 2]
+            q.check(q.ck_decode_layer(out, x, x, Lr["wq"], Lr["wk"], Lr["wv"], Lr["wo"], Lr["gamma"], Lr["bq"],
+                                      Lr["bk"], Lr["bv"], Lr["bo"], Lr["kc"], Lr["vc"], cosd, sind, w.pos, w.D, w.H,
+                                      w.KV, w.hd, w.capacity, w.eps, scratch, nbytes, stream.cuda_stream))
+            x = out
+
+    with torch.cuda.stream(stream):
+        token()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        token()
+    K, W = args.steps, max(args.warmup, 3)
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(K):
+        g.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    per_tok = w.layers * step_bytes(w)
+    peak, peak_kind = measured_peaks()
+    ach = per_tok * ws * K / sec / 1e9
+    return {"metric": METRIC, "value": round(ws * K / sec, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": W, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 dot (dp4a) + fp32", "data": "synthetic",
+            "config": {"workload": "stack32k: 28 layers of the D=3584 28/4-head layer, one token at pos 32768, "
+                                   "one CUDA graph per token", "l2": "4.3 GB per step >> L2"},
+            "step_hbm_gbs": round(ach, 1), "step_bytes": per_tok,
+            "roofline": {"kernel": "whole token step", "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(ach / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": None},
+            "gpu_launches": 4 * w.layers * K, "clocks": clocks}
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+def oracle_steps(w, budget_s: float, max_steps: int | None = None):
+    """Times full oracle decode steps of workload w until budget_s (at least
+    one step) or max_steps.  Returns (steps, seconds)."""
+    import oracle
+    from quantized_weight_attention_gb300 import synth
+    L = synth.make_layer(w)
+    cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+    kc, vc = L.k_cache.copy(), L.v_cache.copy()
+    oracle.lib()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_layer(L.x, L.x, L.wq, L.wk, L.wv, L.wo, L.gamma, L.bq, L.bk, L.bv, L.bo, kc, vc, cos, sin,
+                            w.pos, w.D, w.H, w.KV, w.hd, w.capacity, w.eps)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps is not None and n >= max_steps):
+            return n, el
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(w, budget_s):
+    n, el = oracle_steps(w, budget_s)
+    return {"value": round(n / el, 3), "unit": "layer-steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full decode steps of the {w.name} layer by the single-threaded C oracle "
+                      f"(double accumulation), {el:.1f} s, cpu: {cpu_model()}"}
+
+
+def run_reference(args, ws):
+    from quantized_weight_attention_gb300 import synth
+    w = synth.WORKLOADS[args.config]
+    # each step is one full oracle decode step; the number timed is capped so
+    # that warm-up + timed steps end within a few minutes
+    budget = 150.0
+    _, per = oracle_steps(w, 0.0, max_steps=1)
+    per = max(per, 1e-6)
+    W = min(max(args.warmup, 0), int(20.0 / per))
+    if W:
+        oracle_steps(w, 1e9, max_steps=W)
+    K = max(1, min(args.steps, int(budget / per)))
+    n, el = oracle_steps(w, 1e9, max_steps=K)
+    v = n / el
+    unit = "tokens/s" if args.config == "stack32k" else "layer-steps/s"
+    if args.config == "stack32k":
+        v /= w.layers
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": unit, "n_gpus": ws, "steps": n,
+            "warmup": W, "ms_per_step": round(1e3 * el / n, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 accumulation (C oracle)", "data": "synthetic",
+            "config": {"workload": f"{w.name} (same as the GPU arm)",
+                       "note": f"{n} of the requested {args.steps} steps timed to stay within {budget:.0f} s"},
+            "cpu_baseline": {"value": round(v, 4), "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": f"{n} full decode layer steps, single-threaded, cpu: {cpu_model()}"},
+            "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":  # rank 0 alone; the other ranks exit without work
+        ws, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            print(json.dumps(run_reference(args, ws)), flush=True)
+        return
+    ws, rank, local, pg = dist_setup()
+    line = run_ours(args, ws, rank, local, pg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
