@@ -2,16 +2,18 @@
 // major_gqa_flash of the page "mega_fused_attention_decode_q5_0.c" (STEP 7),
 // as split-KV flash decoding:
 //
-//   k_attn_split    grid (S splits, KV heads, B sequences).  One CTA owns
-//                   rows [t0, t1) of one KV head and all G = H/KV query heads
-//                   that read it ("GQA-packed": each cache row is read once
-//                   per KV head).  K and V tiles of 32 rows stream into a
-//                   3-stage shared-memory ring through the bulk-copy engine;
-//                   online softmax over the tiles; writes (m, l, acc) per
-//                   query head.
-//   k_attn_combine  grid (H, B).  Log-sum-exp merge of the S partials of one
-//                   query head, the fp32 output, and its Q8_0 quantization
-//                   (the O projection's input) in the epilogue.
+//   k_attn_split    grid (S splits, KV heads, B sequences), one CTA per SM.
+//                   One CTA owns rows [t0, t1) of one KV head and all G =
+//                   H/KV query heads that read it ("GQA-packed": each cache
+//                   row is read once per KV head).  A producer warp streams
+//                   16-row K and V tiles into a deep shared-memory ring
+//                   through the bulk-copy engine; eight consumer warps take
+//                   tiles round-robin, each with its own online softmax;
+//                   writes (m, l, acc) per query head.
+//   k_attn_combine  grid (H, hd/32, B).  Log-sum-exp merge of the S partials
+//                   of one query head over one 32-wide slice of its dims,
+//                   the fp32 output, and its Q8_0 block (the O projection's
+//                   input) in the epilogue.
 //
 // Scores are kept in log2 units: s2 = (q.k) * log2(e)/sqrt(hd), weights
 // exp2(s2 - m2), which equals exp(s - m) of the definition.
@@ -22,32 +24,37 @@
 
 namespace ck {
 
-constexpr int ATT_TILE = 32;
-constexpr int ATT_WARPS = 4;
-constexpr int ATT_THREADS = 32 * ATT_WARPS;
-constexpr int GMAX = 8;  // query heads per KV head handled by one CTA
+constexpr int AT_TILE = 16;                          // cache rows per stage
+constexpr int AT_CONSUMERS = 8;                      // consumer warps per CTA
+constexpr int AT_THREADS = 32 * (AT_CONSUMERS + 1);  // + one producer warp
+constexpr int GMAX = 8;                              // query heads per KV head
 
-__host__ __device__ constexpr int att_stages(int hd) { return hd > 128 ? 2 : 3; }
+__host__ __device__ constexpr int at_stage_bytes(int hd) { return 2 * AT_TILE * hd * 4; }
+__host__ __device__ constexpr int at_stages(int hd) {
+    return (192 * 1024) / at_stage_bytes(hd) > 16 ? 16 : (192 * 1024) / at_stage_bytes(hd);
+}
 
 struct AttnSmem {
-    size_t off_bar, off_stage, off_q, off_s, off_p, off_ml, total;
+    size_t off_full, off_empty, off_stage, off_q, off_p, off_alpha, off_ml, total;
 };
 
 __host__ __device__ inline AttnSmem attn_smem(int hd) {
     AttnSmem L;
     size_t o = 0;
-    L.off_bar = o;
-    o += 64;
+    L.off_full = o;
+    o += 16 * 8;
+    L.off_empty = o;
+    o += 16 * 8;
     L.off_stage = o;
-    o += static_cast<size_t>(att_stages(hd)) * 2 * ATT_TILE * hd * 4;
+    o += static_cast<size_t>(at_stages(hd)) * at_stage_bytes(hd);
     L.off_q = o;
     o += static_cast<size_t>(GMAX) * hd * 4;
-    L.off_s = o;
-    o += GMAX * ATT_TILE * 4;
     L.off_p = o;
-    o += ATT_TILE * GMAX * 4;
+    o += static_cast<size_t>(AT_CONSUMERS) * AT_TILE * GMAX * 4;
+    L.off_alpha = o;
+    o += static_cast<size_t>(AT_CONSUMERS) * GMAX * 4;
     L.off_ml = o;
-    o += 4 * GMAX * 4;  // m, l, alpha, spare
+    o += static_cast<size_t>(2) * AT_CONSUMERS * GMAX * 4;
     L.total = (o + 127) / 128 * 128;
     return L;
 }
@@ -60,21 +67,38 @@ size_t attn_part_bytes(int B, int H, int KV, int hd, int splits) {
     return static_cast<size_t>(B) * KV * splits * part_stride(G, hd) * 4;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sptr(bar)) : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_CONSUMERS) : "memory");
+}
+
+// One CTA per (split s, KV head g, sequence b); one CTA per SM.  Warp 0 is
+// the producer: its lane 0 streams 16-row K and V tiles of rows [t0, t1)
+// into an NST-stage ring (full / empty mbarrier per stage).  Warps 1..8
+// consume tiles round-robin, each keeping its own online-softmax state for
+// the G query heads; no CTA-wide barrier inside the loop.  At the end the
+// eight states are merged (log-sum-exp) into the split's record.
+//
+// Scores: lane = (slice = lane & 7, row-lane rl = lane >> 3).  A slice is
+// the float4 chunks {slice + 8c} of a row (interleaved so that the 8 slices
+// hit 8 different bank groups); a lane accumulates 4 rows (rl + 4k) x G
+// heads over its slice, then the 8 slices are summed with xor shuffles.
+// Lane (slice = j, rl) then owns query head j's softmax state.
 template <int DPL>
-__global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_split(const AttnArgs a) {
+__global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) {
     constexpr int HD = 32 * DPL;
     constexpr int HD4 = HD / 4;
-    constexpr int NST = att_stages(HD);
+    constexpr int NST = at_stages(HD);
     constexpr int VEC = (DPL % 4 == 0) ? 4 : ((DPL % 2 == 0) ? 2 : 1);
     constexpr int NV = DPL / VEC;
     extern __shared__ __align__(128) uint8_t smem[];
     const AttnSmem L = attn_smem(HD);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.off_empty);
     float *stage = reinterpret_cast<float *>(smem + L.off_stage);
     float *qs = reinterpret_cast<float *>(smem + L.off_q);
-    float *Ss = reinterpret_cast<float *>(smem + L.off_s);   // [GMAX][TILE]
-    float *Ps = reinterpret_cast<float *>(smem + L.off_p);   // [TILE][GMAX]
-    float *ml = reinterpret_cast<float *>(smem + L.off_ml);  // m[GMAX], l[GMAX], alpha[GMAX]
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int S = gridDim.x;
@@ -82,17 +106,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_split(const AttnArgs a)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // Spread an L2 prefetch of the next kernel's operand over the grid.
-    const uint8_t *l2_pf = static_cast<const uint8_t *>(a.l2_prefetch);
-    const size_t l2_pf_bytes = a.l2_prefetch_bytes & ~static_cast<size_t>(15);
-    if (l2_pf && threadIdx.x == 0) {
+    if (a.l2_prefetch && threadIdx.x == 0) {
+        const uint8_t *pf = static_cast<const uint8_t *>(a.l2_prefetch);
+        const size_t total = a.l2_prefetch_bytes & ~static_cast<size_t>(15);
         const size_t nct = static_cast<size_t>(gridDim.x) * gridDim.y * gridDim.z;
         const size_t cid = (static_cast<size_t>(b) * gridDim.y + g) * gridDim.x + s;
-        const size_t per = ((l2_pf_bytes + nct - 1) / nct + 15) & ~static_cast<size_t>(15);
+        const size_t per = ((total + nct - 1) / nct + 15) & ~static_cast<size_t>(15);
         const size_t beg = cid * per;
-        if (beg < l2_pf_bytes) {
-            size_t n = l2_pf_bytes - beg < per ? l2_pf_bytes - beg : per;
-            n &= ~static_cast<size_t>(15);
-            if (n) prefetch_l2(l2_pf + beg, static_cast<uint32_t>(n));
+        if (beg < total) {
+            const size_t n = (total - beg < per ? total - beg : per) & ~static_cast<size_t>(15);
+            if (n) prefetch_l2(pf + beg, static_cast<uint32_t>(n));
         }
     }
 
@@ -108,7 +131,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_split(const AttnArgs a)
     } else {
         T = a.kv_tokens;
     }
-    const int chunk = (T + S - 1) / S;
+    const int chunk = a.chunk > 0 ? a.chunk : (T + S - 1) / S;
     const int t0 = s * chunk;
     const int t1 = min(T, t0 + chunk);
     float *rec = a.part + ((static_cast<size_t>(b) * a.KV + g) * S + s) * part_stride(G, HD);
@@ -123,152 +146,175 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_split(const AttnArgs a)
     }
     const float *kc = (a.k_caches ? a.k_caches[b] : a.k_cache) + static_cast<size_t>(g) * a.C * HD;
     const float *vc = (a.v_caches ? a.v_caches[b] : a.v_cache) + static_cast<size_t>(g) * a.C * HD;
-    const int ntiles = (t1 - t0 + ATT_TILE - 1) / ATT_TILE;
+    const int ntiles = (t1 - t0 + AT_TILE - 1) / AT_TILE;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
-    // Tile i of this split -> stage i % NST.  Rows before T-1 are never
-    // written by the preceding grid, so they are fetched before waiting on
-    // it; the tile holding row T-1 (the row just stored) waits first.
-    auto issue = [&](int i) {
-        const int r = t0 + i * ATT_TILE;
-        const int n = min(ATT_TILE, t1 - r);
-        if (r + n >= T) pdl_wait();
-        float *dst = stage + static_cast<size_t>(i % NST) * 2 * ATT_TILE * HD;
-        const uint32_t bytes = static_cast<uint32_t>(n) * HD * 4;
-        mbar_arrive_expect_tx(&bars[i % NST], 2 * bytes);
-        bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &bars[i % NST]);
-        bulk_g2s(dst + ATT_TILE * HD, vc + static_cast<size_t>(r) * HD, bytes, &bars[i % NST]);
-    };
-    if (threadIdx.x == 0)
-        for (int i = 0; i < NST && i < ntiles; ++i) issue(i);
-
     pdl_trigger();
-    pdl_wait();  // q is the preceding grid's output
-    for (int idx = threadIdx.x; idx < G * HD; idx += ATT_THREADS)
-        qs[idx] = a.q[(static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * HD + idx];
-    if (threadIdx.x < GMAX) {
-        ml[threadIdx.x] = -INFINITY;
-        ml[GMAX + threadIdx.x] = 0.0f;
+
+    if (warp == 0) {
+        // ---- producer.  Rows before T-1 are never written by the preceding
+        // grid, so they stream before waiting on it; the tile holding row
+        // T-1 (the row just stored) waits first.
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t % NST;
+                if (t >= NST && !mbar_wait(&empty[st], ((t / NST) - 1) & 1)) {
+                    flag_error(a.status, FLAG_TIMEOUT);
+                    break;
+                }
+                const int r = t0 + t * AT_TILE;
+                const int n = min(AT_TILE, t1 - r);
+                if (r + n >= T) pdl_wait();
+                float *dst = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
+                const uint32_t bytes = static_cast<uint32_t>(n) * HD * 4;
+                mbar_arrive_expect_tx(&full[st], 2 * bytes);
+                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &full[st]);
+                bulk_g2s(dst + AT_TILE * HD, vc + static_cast<size_t>(r) * HD, bytes, &full[st]);
+            }
+        }
+        return;
     }
-    __syncthreads();
+
+    // ---- consumers
+    const int cw = warp - 1;
+    const int ct = threadIdx.x - 32;
+    float *Pw = reinterpret_cast<float *>(smem + L.off_p) + cw * AT_TILE * GMAX;  // [TILE][GMAX]
+    float *alw = reinterpret_cast<float *>(smem + L.off_alpha) + cw * GMAX;
+    float *mlw = reinterpret_cast<float *>(smem + L.off_ml);  // m[NC][GMAX], l[NC][GMAX]
+    pdl_wait();  // q is the preceding grid's output
+    for (int idx = ct; idx < G * HD; idx += 32 * AT_CONSUMERS)
+        qs[idx] = a.q[(static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * HD + idx];
+    consumers_sync();
 
     const float scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
     const float4 *q4 = reinterpret_cast<const float4 *>(qs);
+    const int slice = lane & 7, rl = lane >> 3;
+    float mrun = -INFINITY, lrun = 0.0f;  // head `slice`
     float acc[GMAX][DPL];
 #pragma unroll
     for (int j = 0; j < GMAX; ++j)
 #pragma unroll
         for (int e = 0; e < DPL; ++e) acc[j][e] = 0.0f;
 
-    const int slice = lane & 7, rl = lane >> 3;
-    const int rA = 8 * warp + rl, rB = rA + 4;
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % NST;
-        if (!mbar_wait(&bars[st], (i / NST) & 1)) flag_error(a.status, FLAG_TIMEOUT);
-        const float *Kt = stage + static_cast<size_t>(st) * 2 * ATT_TILE * HD;
-        const float *Vt = Kt + ATT_TILE * HD;
-        const int n = min(ATT_TILE, t1 - (t0 + i * ATT_TILE));
+    for (int t = cw; t < ntiles; t += AT_CONSUMERS) {
+        const int st = t % NST;
+        if (!mbar_wait(&full[st], (t / NST) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+        const float *Kt = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
+        const float *Vt = Kt + AT_TILE * HD;
+        const int n = min(AT_TILE, t1 - (t0 + t * AT_TILE));
 
-        // ---- scores: lane = (row pair, 1/8 of the dims, float4-interleaved)
-        {
-            const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
-            float sa[GMAX], sb[GMAX];
+        float sc[GMAX][4];
 #pragma unroll
-            for (int j = 0; j < GMAX; ++j) sa[j] = sb[j] = 0.0f;
+        for (int j = 0; j < GMAX; ++j)
 #pragma unroll
-            for (int c = 0; c < DPL; ++c) {
-                const float4 ka = K4[rA * HD4 + slice + 8 * c];
-                const float4 kb = K4[rB * HD4 + slice + 8 * c];
+            for (int k = 0; k < 4; ++k) sc[j][k] = 0.0f;
+        const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
 #pragma unroll
-                for (int j = 0; j < GMAX; ++j) {
-                    if (j < G) {
-                        const float4 qv = q4[j * HD4 + slice + 8 * c];
-                        sa[j] = fmaf(qv.x, ka.x, fmaf(qv.y, ka.y, fmaf(qv.z, ka.z, fmaf(qv.w, ka.w, sa[j]))));
-                        sb[j] = fmaf(qv.x, kb.x, fmaf(qv.y, kb.y, fmaf(qv.z, kb.z, fmaf(qv.w, kb.w, sb[j]))));
-                    }
-                }
-            }
+        for (int c = 0; c < DPL; ++c) {
+            float4 kk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) kk[k] = K4[(rl + 4 * k) * HD4 + slice + 8 * c];
 #pragma unroll
             for (int j = 0; j < GMAX; ++j) {
+                if (j < G) {
+                    const float4 qv = q4[j * HD4 + slice + 8 * c];
 #pragma unroll
-                for (int o = 1; o < 8; o <<= 1) {
-                    sa[j] += __shfl_xor_sync(0xffffffffu, sa[j], o);
-                    sb[j] += __shfl_xor_sync(0xffffffffu, sb[j], o);
+                    for (int k = 0; k < 4; ++k)
+                        sc[j][k] = fmaf(qv.x, kk[k].x,
+                                        fmaf(qv.y, kk[k].y, fmaf(qv.z, kk[k].z, fmaf(qv.w, kk[k].w, sc[j][k]))));
                 }
             }
-            float va = 0.0f, vb = 0.0f;
+        }
+#pragma unroll
+        for (int j = 0; j < GMAX; ++j) {
+            if (j < G) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    sc[j][k] += __shfl_xor_sync(0xffffffffu, sc[j][k], 1);
+                    sc[j][k] += __shfl_xor_sync(0xffffffffu, sc[j][k], 2);
+                    sc[j][k] += __shfl_xor_sync(0xffffffffu, sc[j][k], 4);
+                }
+            }
+        }
+        // this lane's head j = slice, rows rl + 4k
+        float my[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float v = 0.0f;
 #pragma unroll
             for (int j = 0; j < GMAX; ++j)
-                if (j == slice) {
-                    va = sa[j];
-                    vb = sb[j];
-                }
-            if (slice < G) {
-                Ss[slice * ATT_TILE + rA] = rA < n ? va * scale2 : -INFINITY;
-                Ss[slice * ATT_TILE + rB] = rB < n ? vb * scale2 : -INFINITY;
-            }
+                if (j == slice) v = sc[j][k];
+            my[k] = (rl + 4 * k < n) ? v * scale2 : -INFINITY;
         }
-        __syncthreads();
-        // ---- online softmax update, one warp per query head
-        for (int j = warp; j < G; j += ATT_WARPS) {
-            const float x = Ss[j * ATT_TILE + lane];
-            const float mo = ml[j];
-            const float mn = fmaxf(mo, warp_max(x));
-            const float alpha = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
-            const float p = (x == -INFINITY) ? 0.0f : exp2f(x - mn);
-            Ps[lane * GMAX + j] = p;
-            const float ps = warp_sum(p);
-            if (lane == 0) {
-                ml[GMAX + j] = ml[GMAX + j] * alpha + ps;
-                ml[j] = mn;
-                ml[2 * GMAX + j] = alpha;
-            }
-        }
-        __syncthreads();
-        // ---- acc = alpha * acc + P V over this warp's 8 rows
-        {
+        float tmax = fmaxf(fmaxf(my[0], my[1]), fmaxf(my[2], my[3]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float mnew = fmaxf(mrun, tmax);
+        const float alpha = (mrun == -INFINITY) ? 0.0f : exp2f(mrun - mnew);
+        float psum = 0.0f;
 #pragma unroll
-            for (int j = 0; j < GMAX; ++j) {
-                const float al = (j < G) ? ml[2 * GMAX + j] : 0.0f;
+        for (int k = 0; k < 4; ++k) {
+            const float p = (my[k] == -INFINITY || slice >= G) ? 0.0f : exp2f(my[k] - mnew);
+            Pw[(rl + 4 * k) * GMAX + slice] = p;
+            psum += p;
+        }
+        psum += __shfl_xor_sync(0xffffffffu, psum, 8);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 16);
+        lrun = lrun * alpha + psum;
+        mrun = mnew;
+        if (rl == 0) alw[slice] = alpha;
+        __syncwarp();
+        // ---- acc = alpha * acc + P V
+#pragma unroll
+        for (int j = 0; j < GMAX; ++j) {
+            if (j < G) {
+                const float al = alw[j];
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) acc[j][e] *= al;
             }
-            const int rend = min(8 * warp + 8, n);
-            for (int r = 8 * warp; r < rend; ++r) {
-                const float4 p0 = reinterpret_cast<const float4 *>(Ps + r * GMAX)[0];
-                const float4 p1 = reinterpret_cast<const float4 *>(Ps + r * GMAX)[1];
-                const float pj[GMAX] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                float v[DPL];
-#pragma unroll
-                for (int u = 0; u < NV; ++u) {
-                    const float *src = Vt + r * HD + VEC * (lane + 32 * u);
-                    if constexpr (VEC == 4) {
-                        const float4 t = *reinterpret_cast<const float4 *>(src);
-                        v[4 * u] = t.x; v[4 * u + 1] = t.y; v[4 * u + 2] = t.z; v[4 * u + 3] = t.w;
-                    } else if constexpr (VEC == 2) {
-                        const float2 t = *reinterpret_cast<const float2 *>(src);
-                        v[2 * u] = t.x; v[2 * u + 1] = t.y;
-                    } else {
-                        v[u] = *src;
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < GMAX; ++j)
-                    if (j < G)
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e) acc[j][e] = fmaf(pj[j], v[e], acc[j][e]);
-            }
         }
-        __syncthreads();  // stage st, Ss and Ps are free again
-        if (threadIdx.x == 0 && i + NST < ntiles) issue(i + NST);
+        for (int r = 0; r < n; ++r) {
+            const float4 p0 = reinterpret_cast<const float4 *>(Pw + r * GMAX)[0];
+            const float4 p1 = reinterpret_cast<const float4 *>(Pw + r * GMAX)[1];
+            const float pj[GMAX] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            float v[DPL];
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const float *src = Vt + r * HD + VEC * (lane + 32 * u);
+                if constexpr (VEC == 4) {
+                    const float4 tv = *reinterpret_cast<const float4 *>(src);
+                    v[4 * u] = tv.x; v[4 * u + 1] = tv.y; v[4 * u + 2] = tv.z; v[4 * u + 3] = tv.w;
+                } else if constexpr (VEC == 2) {
+                    const float2 tv = *reinterpret_cast<const float2 *>(src);
+                    v[2 * u] = tv.x; v[2 * u + 1] = tv.y;
+                } else {
+                    v[u] = *src;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < GMAX; ++j)
+                if (j < G)
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[j][e] = fmaf(pj[j], v[e], acc[j][e]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
     }
 
-    // ---- merge the 4 warps' accumulators (stage memory is idle now)
-    float *red = stage;  // [ATT_WARPS][G][HD]
+    // ---- merge the consumer warps' states
+    if (rl == 0 && slice < G) {
+        mlw[cw * GMAX + slice] = mrun;
+        mlw[(AT_CONSUMERS + cw) * GMAX + slice] = lrun;
+    }
+    consumers_sync();  // every tile consumed: the ring is idle
+    float *accw = stage;  // [NC][G][HD]
 #pragma unroll
     for (int j = 0; j < GMAX; ++j)
         if (j < G)
@@ -276,30 +322,43 @@ __global__ void __launch_bounds__(ATT_THREADS, 2) k_attn_split(const AttnArgs a)
             for (int u = 0; u < NV; ++u)
 #pragma unroll
                 for (int e = 0; e < VEC; ++e)
-                    red[(warp * G + j) * HD + VEC * (lane + 32 * u) + e] = acc[j][VEC * u + e];
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * HD; idx += ATT_THREADS) {
+                    accw[(cw * G + j) * HD + VEC * (lane + 32 * u) + e] = acc[j][VEC * u + e];
+    consumers_sync();
+    for (int idx = ct; idx < G * HD; idx += 32 * AT_CONSUMERS) {
+        const int j = idx / HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < AT_CONSUMERS; ++w) M = fmaxf(M, mlw[w * GMAX + j]);
         float t = 0.0f;
 #pragma unroll
-        for (int w = 0; w < ATT_WARPS; ++w) t += red[w * G * HD + idx];
+        for (int w = 0; w < AT_CONSUMERS; ++w) {
+            const float mw = mlw[w * GMAX + j];
+            if (mw != -INFINITY) t = fmaf(exp2f(mw - M), accw[(w * G + j) * HD + (idx - j * HD)], t);
+        }
         rec[2 * G + idx] = t;
-    }
-    if (threadIdx.x < G) {
-        rec[threadIdx.x] = ml[threadIdx.x];
-        rec[G + threadIdx.x] = ml[GMAX + threadIdx.x];
+        if (idx - j * HD == 0) {
+            float Ls = 0.0f;
+#pragma unroll
+            for (int w = 0; w < AT_CONSUMERS; ++w) {
+                const float mw = mlw[w * GMAX + j];
+                if (mw != -INFINITY) Ls = fmaf(exp2f(mw - M), mlw[(AT_CONSUMERS + w) * GMAX + j], Ls);
+            }
+            rec[j] = M;
+            rec[G + j] = Ls;
+        }
     }
 }
 
-// Merge of the S partial records of one query head; fp32 output and its
-// Q8_0 blocks.
+// Merge of the S partial records of one query head, for one 32-wide slice of
+// its dims (= one Q8_0 block of the output): fp32 output and the block.
 template <int DPL>
 __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
     constexpr int HD = 32 * DPL;
     constexpr int NW = 8;
-    __shared__ float red[NW][HD];
+    constexpr int U = 4;
+    __shared__ float ared[NW][32];
     __shared__ float lred[NW];
-    __shared__ float o_s[HD];
-    const int h = blockIdx.x, b = blockIdx.y;
+    const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
     const int G = a.H / a.KV;
     const int g = h / G, j = h - g * G;
     const int S = a.splits;
@@ -318,45 +377,48 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, base[s * ps + j]);
     M = warp_max(M);
-    float acc[DPL];
+    float acc = 0.0f, Ls = 0.0f;
+    for (int s0 = warp; s0 < S; s0 += NW * U) {
+        float mv[U], lv[U], av[U];
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[e] = 0.0f;
-    float Ls = 0.0f;
-    for (int s = warp; s < S; s += NW) {
-        const float *r = base + s * ps;
-        const float ms = r[j];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - M);
-        Ls = fmaf(w, r[G + j], Ls);
-        const float *ac = r + 2 * G + static_cast<size_t>(j) * HD;
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + NW * u;
+            const bool ok = s < S;
+            const float *r = base + static_cast<size_t>(ok ? s : 0) * ps;
+            mv[u] = ok ? r[j] : -INFINITY;
+            lv[u] = ok ? r[G + j] : 0.0f;
+            av[u] = ok ? r[2 * G + j * HD + blk * 32 + lane] : 0.0f;
+        }
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, ac[lane + 32 * e], acc[e]);
+        for (int u = 0; u < U; ++u) {
+            const bool live = mv[u] != -INFINITY;
+            const float w = live ? exp2f(mv[u] - M) : 0.0f;
+            Ls = fmaf(w, live ? lv[u] : 0.0f, Ls);
+            acc = fmaf(w, live ? av[u] : 0.0f, acc);
+        }
     }
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) red[warp][lane + 32 * e] = acc[e];
+    ared[warp][lane] = acc;
     if (lane == 0) lred[warp] = Ls;
     __syncthreads();
-    float L = 0.0f;
+    if (warp == 0) {
+        float t = 0.0f, L = 0.0f;
 #pragma unroll
-    for (int w = 0; w < NW; ++w) L += lred[w];
-    for (int d = threadIdx.x; d < HD; d += blockDim.x) {
-        float t = 0.0f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) t += red[w][d];
+        for (int w = 0; w < NW; ++w) {
+            t += ared[w][lane];
+            L += lred[w];
+        }
         const float o = __fdiv_rn(t, L);
-        o_s[d] = o;
-        a.out[(static_cast<size_t>(b) * a.H + h) * HD + d] = o;
-    }
-    __syncthreads();
-    if (a.out_q8 && warp < HD / 32) {
-        uint32_t dbits;
-        float dq;
-        const int q = q8_code(o_s[32 * warp + lane], dbits, dq);
-        uint8_t *blk = a.out_q8 + ((static_cast<size_t>(b) * a.H + h) * (HD / 32) + warp) * Q8B;
-        blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-        if (lane == 0) {
-            blk[0] = static_cast<uint8_t>(dbits & 0xFF);
-            blk[1] = static_cast<uint8_t>(dbits >> 8);
+        a.out[(static_cast<size_t>(b) * a.H + h) * HD + blk * 32 + lane] = o;
+        if (a.out_q8) {
+            uint32_t dbits;
+            float dq;
+            const int q = q8_code(o, dbits, dq);
+            uint8_t *qb = a.out_q8 + ((static_cast<size_t>(b) * a.H + h) * (HD / 32) + blk) * Q8B;
+            qb[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+            if (lane == 0) {
+                qb[0] = static_cast<uint8_t>(dbits & 0xFF);
+                qb[1] = static_cast<uint8_t>(dbits >> 8);
+            }
         }
     }
 }
@@ -391,10 +453,9 @@ __global__ void k_kv_store(float *kc, float *vc, const float *__restrict__ k, co
 // Host side
 // ---------------------------------------------------------------------------
 int attn_splits(int B, int KV, int max_tokens) {
-    const int nsm = device_info().num_sms;
-    const int ctas = 2 * nsm;  // two CTAs fit per SM
-    int S = (ctas + B * KV - 1) / (B * KV);
-    const int tiles = (max_tokens + ATT_TILE - 1) / ATT_TILE;
+    const int nsm = device_info().num_sms;  // one CTA per SM
+    int S = (nsm + B * KV - 1) / (B * KV);
+    const int tiles = (max_tokens + AT_TILE - 1) / AT_TILE;
     if (S > tiles) S = tiles;
     if (S < 1) S = 1;
     if (S > 1024) S = 1024;
@@ -408,10 +469,10 @@ static int launch_attn_t(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_fir
     const void *fs = reinterpret_cast<const void *>(k_attn_split<DPL>);
     ensure_smem(fs, L.total);
     void *args1[] = {&a};
-    cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(ATT_THREADS), L.total, s, pdl_first, args1);
+    cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(AT_THREADS), L.total, s, pdl_first, args1);
     if (e != cudaSuccess) return -5;
     void *args2[] = {&a};
-    e = launch(reinterpret_cast<const void *>(k_attn_combine<DPL>), dim3(a.H, B), dim3(256), 0, s, pdl_combine,
+    e = launch(reinterpret_cast<const void *>(k_attn_combine<DPL>), dim3(a.H, DPL, B), dim3(256), 0, s, pdl_combine,
                args2);
     return e == cudaSuccess ? 0 : -5;
 }

@@ -25,7 +25,7 @@ namespace ck {
 // Shared-memory plan of a projection CTA (identical on host and device)
 // ---------------------------------------------------------------------------
 struct ProjSmem {
-    size_t off_w, off_xq, off_xd, off_xs, off_part, off_rowsum, off_red, total;
+    size_t off_w, off_xq, off_xd, off_xs, off_part, off_rowsum, off_red, off_raw, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -34,7 +34,7 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // weight rows (0 on the direct path).
 __host__ __device__ inline ProjSmem proj_smem(int R, int nb, size_t wbytes) {
     ProjSmem s;
-    size_t o = 128;  // mbarriers (up to 8)
+    size_t o = 128;  // mbarriers (up to 16)
     s.off_w = o;
     o = align_up(o + wbytes, 16);
     s.off_xq = o;
@@ -50,6 +50,8 @@ __host__ __device__ inline ProjSmem proj_smem(int R, int nb, size_t wbytes) {
     o += static_cast<size_t>(R) * 4;
     s.off_red = o;
     o += 64 * 4;
+    s.off_raw = o;  // raw bytes of a Q8_0 activation row
+    o = align_up(o + static_cast<size_t>(nb) * Q8B + 16, 16);
     s.total = align_up(o, 128);
     return s;
 }
@@ -59,11 +61,36 @@ __host__ __device__ inline int row_stride(int nb, bool q8) { return nb * (q8 ? Q
 // ---------------------------------------------------------------------------
 // Activation prologues
 // ---------------------------------------------------------------------------
-// Q8_0 blocks already in global memory -> XRow in shared memory.
-__device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x) {
+// Q8_0 blocks already in global memory (4-byte aligned) -> XRow in shared
+// memory.  Every global load of the row is issued before any is used (a few
+// 32-bit words per thread), then the blocks are unpacked from shared memory.
+// `raw` holds nb*34 bytes (+ slack).
+__device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x, uint32_t *raw) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int bytes = nb * Q8B;  // even
+    const int words = bytes >> 2;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(xq8);
+    constexpr int U = 4;
+    for (int base = 0; base < words; base += U * static_cast<int>(blockDim.x)) {
+        uint32_t v[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int i = base + k * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            v[k] = i < words ? __ldg(src + i) : 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int i = base + k * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            if (i < words) raw[i] = v[k];
+        }
+    }
+    if ((bytes & 2) && threadIdx.x == 0)
+        reinterpret_cast<uint16_t *>(raw)[(bytes >> 1) - 1] =
+            __ldg(reinterpret_cast<const unsigned short *>(xq8) + (bytes >> 1) - 1);
+    __syncthreads();
+    const uint8_t *rb = reinterpret_cast<const uint8_t *>(raw);
     for (int b = warp; b < nb; b += nw) {
-        const uint8_t *p = xq8 + static_cast<size_t>(b) * Q8B;
+        const uint8_t *p = rb + b * Q8B;
         const int c = static_cast<int8_t>(p[2 + lane]);
         const int sum = warp_isum(c);
         reinterpret_cast<int8_t *>(&x.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(c);
@@ -79,18 +106,35 @@ __device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x) {
 // exact FMA residual of each square), so it equals the double-precision sum
 // to ~2^-46 relative; rstd = 1/sqrt(mean + eps) is then formed in double
 // and rounded once to fp32, and y = (x * rstd) * gamma in fp32.
+//
+// Thread (warp w, lane l) owns element l of blocks w + nw*k.  With at most
+// PB blocks per warp (D <= 32*nw*PB) x and gamma are loaded once, all loads
+// in flight together, and kept in registers for the quantization pass.
 __device__ void xrow_rmsnorm_q8(const float *x, const float *gamma, float eps, int D, const XRow &xr, float *red,
                                 uint8_t *xq8_out) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nb = D / QK;
+    constexpr int PB = 8;
+    const bool keep = nb <= nw * PB;
+    float xv[PB], gv[PB];
     float s = 0.0f, c = 0.0f;
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-        const float v = x[i];
-        const float p = __fmul_rn(v, v);
-        const float e = fmaf(v, v, -p);
-        float t, err;
-        two_sum(s, p, t, err);
-        s = t;
-        c = __fadd_rn(c, __fadd_rn(err, e));
+    for (int r0 = 0; r0 < nb; r0 += nw * PB) {
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+            const int b = r0 + warp + nw * k;
+            xv[k] = b < nb ? x[b * QK + lane] : 0.0f;
+            gv[k] = (keep && b < nb) ? gamma[b * QK + lane] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+            const float v = xv[k];
+            const float p = __fmul_rn(v, v);
+            const float e = fmaf(v, v, -p);
+            float t, err;
+            two_sum(s, p, t, err);
+            s = t;
+            c = __fadd_rn(c, __fadd_rn(err, e));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -125,25 +169,37 @@ __device__ void xrow_rmsnorm_q8(const float *x, const float *gamma, float eps, i
     }
     __syncthreads();
     const float rstd = red[63];
-    const int nb = D / QK;
-    for (int b = warp; b < nb; b += nw) {
-        const int i = b * QK + lane;
-        const float y = __fmul_rn(__fmul_rn(x[i], rstd), gamma[i]);
-        uint32_t dbits;
-        float dq;
-        const int q = q8_code(y, dbits, dq);
-        const int sum = warp_isum(q);
-        reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
-        if (lane == 0) {
-            xr.d[b] = dq;
-            xr.sum[b] = sum;
+    for (int r0 = 0; r0 < nb; r0 += nw * PB) {
+        if (!keep) {
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                const int b = r0 + warp + nw * k;
+                xv[k] = b < nb ? x[b * QK + lane] : 0.0f;
+                gv[k] = b < nb ? gamma[b * QK + lane] : 0.0f;
+            }
         }
-        if (xq8_out) {
-            uint8_t *o = xq8_out + static_cast<size_t>(b) * Q8B;
-            o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-            if (lane == 0) {
-                o[0] = static_cast<uint8_t>(dbits & 0xFF);
-                o[1] = static_cast<uint8_t>(dbits >> 8);
+#pragma unroll
+        for (int k = 0; k < PB; ++k) {
+            const int b = r0 + warp + nw * k;
+            if (b < nb) {  // warp-uniform
+                const float y = __fmul_rn(__fmul_rn(xv[k], rstd), gv[k]);
+                uint32_t dbits;
+                float dq;
+                const int q = q8_code(y, dbits, dq);
+                const int sum = warp_isum(q);
+                reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
+                if (lane == 0) {
+                    xr.d[b] = dq;
+                    xr.sum[b] = sum;
+                }
+                if (xq8_out) {
+                    uint8_t *o = xq8_out + static_cast<size_t>(b) * Q8B;
+                    o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+                    if (lane == 0) {
+                        o[0] = static_cast<uint8_t>(dbits & 0xFF);
+                        o[1] = static_cast<uint8_t>(dbits >> 8);
+                    }
+                }
             }
         }
     }
@@ -273,7 +329,7 @@ __global__ void __launch_bounds__(512) k_gemv(float *__restrict__ y, const uint8
         __syncthreads();
         issue_rows(wsm, rstride, W, rb, rows, bars, rowof);
     }
-    xrow_from_q8(xq8, nb, x);
+    xrow_from_q8(xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
     __syncthreads();
     if constexpr (FAST) {
         tile_segments<Q8>(wsm, rstride, rows, R, nseg, bars, x, part, status);
@@ -294,7 +350,7 @@ __global__ void __launch_bounds__(256) k_block_dots(int32_t *__restrict__ isum, 
     const int nb = K / QK;
     const ProjSmem L = proj_smem(1, nb, 0);
     const XRow x = xrow_at(smem, L);
-    xrow_from_q8(xq8, nb, x);
+    xrow_from_q8(xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
     __syncthreads();
     constexpr int BLK = Q8 ? Q8B : Q5B;
     if (nb % 8 == 0) {
@@ -470,7 +526,7 @@ __global__ void __launch_bounds__(512, 1) k_oproj(const OprojArgs a) {
     }
     pdl_trigger();
     pdl_wait();  // the attention output is ready
-    xrow_from_q8(a.aq8, nb, x);
+    xrow_from_q8(a.aq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
     __syncthreads();
     if constexpr (FAST) {
         tile_segments<false>(wsm, rstride, rows, R, nseg, bars, x, part, a.status);

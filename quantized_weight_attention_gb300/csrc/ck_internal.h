@@ -71,6 +71,7 @@ struct AttnArgs {
     int kv_tokens;            // used when d_pos is null (B == 1)
     int H, KV, hd, C;
     int splits;               // S
+    int chunk;                // rows per split (0: ceil(T / S))
     float *part;              // scratch: partial results
     float *out;               // [B][H*hd] fp32 attention output
     uint8_t *out_q8;          // [B][H*hd/32] Q8_0 blocks, or null
