@@ -119,6 +119,26 @@ int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cach
                        int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
                        size_t scratch_bytes, void *stream);
 
+/* The same attention for callers that cannot allocate device memory -- code
+ * whose device memory belongs to another allocator or a fixed budget, and
+ * decode loops that must not pay for a cudaMalloc, which can synchronize the
+ * device.  The pages have no counterpart: this is a library convenience.
+ * Arguments, requirements and result are those of ck_attn_decode_gqa minus
+ * the scratch: the split-KV partials live in one buffer compiled into the
+ * library, CK_ATTN_NOALLOC_MAX_BYTES of device memory that every GPU which
+ * loads the library keeps until the process exits.  A shape whose partials
+ * need more is rejected with CK_ESCRATCH before anything is enqueued; every supported
+ * shape fits on a 152-SM GB300.  The call allocates nothing.  The first call
+ * on a device looks up the buffer's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the buffer and it keeps the last call's
+ * contents (nothing in it needs to start at zero); calls whose work overlaps
+ * on the GPU (other streams or host threads on the same device) race on it. */
+#define CK_ATTN_NOALLOC_MAX_BYTES (2u * 1024u * 1024u)
+int ck_attn_decode_gqa_noalloc(const float *q, const float *k_cache, const float *v_cache, float *out,
+                               int num_heads, int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim,
+                               void *stream);
+
 /* ---- the whole layer step ---------------------------------------------- */
 
 /* mega_fused_attention_decode_q5_0 (page: MAIN KERNEL).  One token at

@@ -24,7 +24,8 @@ __all__ = [
     "ck_rope_inplace", "ck_kv_store", "ck_attn_scratch_size", "ck_attn_decode_gqa",
     "ck_decode_layer_scratch_size", "ck_decode_layer", "ck_decode_layer_devpos", "ck_device_status",
     "ck_block_dots_q5_0_q8_0", "ck_block_dots_q8_0_q8_0", "LIB_PATH", "ck_decode_layer_scratch_offset",
-    "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8",
+    "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8", "ck_attn_decode_gqa_noalloc",
+    "CK_ATTN_NOALLOC_MAX_BYTES",
 ]
 
 CK_OK, CK_EINVAL, CK_ERANGE, CK_ESCRATCH, CK_EALIGN, CK_ECUDA, CK_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -52,6 +53,7 @@ _SIGS = {
     "ck_kv_store": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "ck_attn_scratch_size": (_SZ, [_I, _I, _I, _I]),
     "ck_attn_decode_gqa": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "ck_attn_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ck_decode_layer_scratch_size": (_SZ, [_I, _I, _I, _I, _I]),
     "ck_decode_layer": (_I, [_P] * 16 + [_I] * 6 + [_F, _P, _SZ, _P]),
     "ck_decode_layer_devpos": (_I, [_P] * 17 + [_I] * 5 + [_F, _P, _SZ, _P]),
@@ -138,6 +140,18 @@ def ck_attn_decode_gqa(q, k_cache, v_cache, out, num_heads: int, num_kv_heads: i
     return lib().ck_attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, num_kv_heads,
                                     kv_tokens, cache_capacity, head_dim, _ptr(scratch), scratch_bytes,
                                     _stream(stream))
+
+
+CK_ATTN_NOALLOC_MAX_BYTES = 2 * 1024 * 1024
+
+
+def ck_attn_decode_gqa_noalloc(q, k_cache, v_cache, out, num_heads: int, num_kv_heads: int, kv_tokens: int,
+                               cache_capacity: int, head_dim: int, stream=None) -> int:
+    """ck_attn_decode_gqa without a scratch argument, for callers that cannot
+    allocate device memory: the partials live in a buffer built into the
+    library (shared by all calls; overlapping calls on the GPU race)."""
+    return lib().ck_attn_decode_gqa_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads,
+                                            num_kv_heads, kv_tokens, cache_capacity, head_dim, _stream(stream))
 
 
 def ck_decode_layer_scratch_size(embed_dim: int, num_heads: int, num_kv_heads: int, head_dim: int,
