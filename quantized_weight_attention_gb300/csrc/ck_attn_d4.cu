@@ -1,0 +1,6 @@
+// Decode attention kernels for head_dim = 128 (see ck_attn_kernels.cuh).
+#include "ck_attn_kernels.cuh"
+
+namespace ck {
+template int launch_attention_dpl<4>(const AttnArgs &, int, cudaStream_t, bool, bool);
+}  // namespace ck

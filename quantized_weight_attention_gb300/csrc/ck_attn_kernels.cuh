@@ -1,0 +1,562 @@
+// Split-KV GQA decode attention kernels (attention_forward_decode_head_major_
+// gqa_flash of the page "mega_fused_attention_decode_q5_0.c", STEP 7) and
+// their host launcher, templated on head_dim / 32 (DPL) and on the query
+// group size G.  Included by one translation unit per DPL.
+//
+//   k_attn_split    grid (S splits, KV heads, B sequences), one CTA per SM.
+//                   One CTA owns rows [t0, t1) of one KV head and all G =
+//                   H/KV query heads that read it ("GQA-packed": each cache
+//                   row is read once per KV head).  A producer warp streams
+//                   16-row K and V tiles into a shared-memory ring through
+//                   the bulk-copy engine, keeping AT_LOOKAHEAD tiles in
+//                   flight (refilled as tiles arrive, so they arrive one
+//                   after another instead of all at the end); six consumer
+//                   warps take tiles round-robin, each with its own online
+//                   softmax, and merge their states at the end.
+//   k_attn_combine  grid (H, hd/32, B).  Log-sum-exp merge of the S partial
+//                   records of one query head over one 32-wide slice of its
+//                   dims (= one Q8_0 block): the fp32 output and the block.
+//
+// Scores are kept in log2 units: s2 = (q.k) * log2(e)/sqrt(hd), weights
+// exp2(s2 - m2), which equals exp(s - m) of the definition.
+#pragma once
+
+#include "ck_device.cuh"
+#include "ck_internal.h"
+
+namespace ck {
+
+constexpr int AT_TILE = 16;                          // cache rows per stage
+constexpr int AT_CONSUMERS = 6;                      // consumer warps per CTA
+constexpr int AT_THREADS = 32 * (AT_CONSUMERS + 1);  // + one producer warp
+constexpr int AT_LOOKAHEAD = 5;                      // tiles in flight per CTA
+constexpr int GMAX = 8;                              // query heads per KV head
+
+// Stage count: as many 16-row K+V stages as fit in 192 KB (at most 18),
+// rounded down to a multiple of AT_CONSUMERS.  Tile t lives in stage
+// t % NST and is consumed by warp t % AT_CONSUMERS; with NST a multiple of
+// AT_CONSUMERS, the warp that waits for tile t on its stage's full barrier
+// is the warp that consumed tile t - NST there, so the barrier is never two
+// phases behind and the parity wait cannot pass on a stale phase.
+__host__ __device__ constexpr int at_stage_bytes(int hd) { return 2 * AT_TILE * hd * 4; }
+__host__ __device__ constexpr int at_stages(int hd) {
+    return ((192 * 1024) / at_stage_bytes(hd) > 18 ? 18 : (192 * 1024) / at_stage_bytes(hd)) / AT_CONSUMERS *
+           AT_CONSUMERS;
+}
+static_assert(at_stages(32) % AT_CONSUMERS == 0 && at_stages(256) >= AT_CONSUMERS, "stage ring");
+static_assert(AT_LOOKAHEAD <= at_stages(256), "look-ahead exceeds the ring");
+// P row stride (floats): G heads, each duplicated into a pair, padded so
+// rows stay 16-byte aligned.
+__host__ __device__ constexpr int at_prow(int G) { return 2 * ((G + 1) & ~1); }
+
+struct AttnSmem {
+    size_t off_full, off_empty, off_qbar, off_stage, off_q, off_p, off_alpha, off_ml, total;
+};
+
+__host__ __device__ inline AttnSmem attn_smem(int hd) {
+    AttnSmem L;
+    size_t o = 0;
+    L.off_full = o;
+    o += 18 * 8;
+    L.off_empty = o;
+    o += 18 * 8;
+    L.off_qbar = o;
+    o += 16;
+    L.off_stage = o;
+    o += static_cast<size_t>(at_stages(hd)) * at_stage_bytes(hd);
+    L.off_q = o;
+    o += static_cast<size_t>(GMAX) * hd * 4;
+    L.off_p = o;
+    o += static_cast<size_t>(AT_CONSUMERS) * AT_TILE * at_prow(GMAX) * 4;
+    L.off_alpha = o;
+    o += static_cast<size_t>(AT_CONSUMERS) * GMAX * 4;
+    L.off_ml = o;
+    o += static_cast<size_t>(2) * AT_CONSUMERS * GMAX * 4;
+    L.total = (o + 127) / 128 * 128;
+    return L;
+}
+
+// Partial results: for (b, g, s) a record of G m's, G l's, G*hd acc's.
+__host__ __device__ inline size_t part_stride(int G, int hd) { return static_cast<size_t>(G) * (hd + 2); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sptr(bar)) : "memory");
+}
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_CONSUMERS) : "memory");
+}
+
+// Reduce-scatter of v[8][4] (8 head slots x 4 rows) over the 8 lanes that
+// share a row-lane (xor 4, 2, 1): afterwards lane `slice` holds, in r[4],
+// the full sums of head `slice` for its 4 rows.
+__device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][4], int slice, float (&r)[4]) {
+    float w[4][4];
+    const bool b2 = slice & 4, b1 = slice & 2, b0 = slice & 1;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float send = b2 ? v[j][k] : v[j + 4][k];
+            const float keep = b2 ? v[j + 4][k] : v[j][k];
+            w[j][k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+    float x[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float send = b1 ? w[j][k] : w[j + 2][k];
+            const float keep = b1 ? w[j + 2][k] : w[j][k];
+            x[j][k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float send = b0 ? x[0][k] : x[1][k];
+        const float keep = b0 ? x[1][k] : x[0][k];
+        r[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+}
+
+// One CTA per (split s, KV head g, sequence b).  GT >= G query heads are
+// computed (heads G..GT-1 get a zero q and zero weight).
+//
+// Scores: lane = (slice = lane & 7, row-lane rl = lane >> 3).  A slice is
+// the float4 chunks {slice + 8c} of a row (interleaved so the 8 slices hit
+// 8 different bank groups); a lane accumulates 4 rows (rl + 4k) x GT heads
+// over its slice with packed fp32x2 FMAs (even / odd dims), then a
+// reduce-scatter over the 8 slices leaves lane (slice = j, rl) with query
+// head j's scores, and that lane owns head j's softmax state.
+// PV: lane = dims; each row adds p_j * v to GT accumulators, two dims per
+// packed FMA.
+template <int DPL, int GT>
+__global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) {
+    constexpr int HD = 32 * DPL;
+    constexpr int HD4 = HD / 4;
+    constexpr int NST = at_stages(HD);
+    constexpr int VEC = (DPL % 4 == 0) ? 4 : ((DPL % 2 == 0) ? 2 : 1);
+    constexpr int NV = DPL / VEC;
+    constexpr int PR = at_prow(GT);
+    extern __shared__ __align__(128) uint8_t smem[];
+    const AttnSmem L = attn_smem(HD);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.off_empty);
+    uint64_t *qbar = reinterpret_cast<uint64_t *>(smem + L.off_qbar);
+    float *stage = reinterpret_cast<float *>(smem + L.off_stage);
+    float *qs = reinterpret_cast<float *>(smem + L.off_q);
+
+    const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int S = gridDim.x;
+    const int G = a.H / a.KV;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // Spread an L2 prefetch of the next kernel's operand over the grid.
+    if (a.l2_prefetch && threadIdx.x == 0) {
+        const uint8_t *pf = static_cast<const uint8_t *>(a.l2_prefetch);
+        const size_t total = a.l2_prefetch_bytes & ~static_cast<size_t>(15);
+        const size_t nct = static_cast<size_t>(gridDim.x) * gridDim.y * gridDim.z;
+        const size_t cid = (static_cast<size_t>(b) * gridDim.y + g) * gridDim.x + s;
+        const size_t per = ((total + nct - 1) / nct + 15) & ~static_cast<size_t>(15);
+        const size_t beg = cid * per;
+        if (beg < total) {
+            const size_t n = (total - beg < per ? total - beg : per) & ~static_cast<size_t>(15);
+            if (n) prefetch_l2(pf + beg, static_cast<uint32_t>(n));
+        }
+    }
+
+    int T;
+    if (a.d_pos) {
+        const int pos = a.d_pos[b];
+        if (pos < 0 || pos >= a.C) {
+            if (s == 0 && g == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
+            pdl_wait();
+            return;
+        }
+        T = pos + 1;
+    } else {
+        T = a.kv_tokens;
+    }
+    const int chunk = a.chunk > 0 ? a.chunk : (T + S - 1) / S;
+    const int t0 = s * chunk;
+    const int t1 = min(T, t0 + chunk);
+    float *rec = a.part + ((static_cast<size_t>(b) * a.KV + g) * S + s) * part_stride(G, HD);
+    if (t0 >= t1) {  // empty split: marked by m = -inf, skipped by the combine
+        pdl_trigger();
+        pdl_wait();  // the record may still be read by an earlier combine
+        if (threadIdx.x < G) {
+            rec[threadIdx.x] = -INFINITY;
+            rec[G + threadIdx.x] = 0.0f;
+        }
+        return;
+    }
+    const float *kc = (a.k_caches ? a.k_caches[b] : a.k_cache) + static_cast<size_t>(g) * a.C * HD;
+    const float *vc = (a.v_caches ? a.v_caches[b] : a.v_cache) + static_cast<size_t>(g) * a.C * HD;
+    const int ntiles = (t1 - t0 + AT_TILE - 1) / AT_TILE;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(qbar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ---- producer.  Rows before T-1 are never written by the preceding
+        // grid, so they stream before waiting on it; the tile holding row
+        // T-1 (the row just stored) waits first.  Tile t is issued once tile
+        // t - AT_LOOKAHEAD has arrived and its stage is free.
+        if (lane == 0) {
+            bool ok = true;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int st = t % NST;
+                if (t >= AT_LOOKAHEAD) {
+                    const int u = t - AT_LOOKAHEAD;
+                    ok = mbar_wait(&full[u % NST], (u / NST) & 1);
+                }
+                if (ok && t >= NST) ok = mbar_wait(&empty[st], ((t / NST) - 1) & 1);
+                if (!ok) {
+                    flag_error(a.status, FLAG_TIMEOUT);
+                    break;
+                }
+                const int r = t0 + t * AT_TILE;
+                const int n = min(AT_TILE, t1 - r);
+                if (r + n >= T) pdl_wait();
+                float *dst = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
+                const uint32_t bytes = static_cast<uint32_t>(n) * HD * 4;
+                mbar_arrive_expect_tx(&full[st], 2 * bytes);
+                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &full[st]);
+                bulk_g2s(dst + AT_TILE * HD, vc + static_cast<size_t>(r) * HD, bytes, &full[st]);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers
+    const int cw = warp - 1;
+    const int ct = threadIdx.x - 32;
+    float *Pw = reinterpret_cast<float *>(smem + L.off_p) + cw * AT_TILE * PR;  // [TILE][PR]
+    float *alw = reinterpret_cast<float *>(smem + L.off_alpha) + cw * GMAX;
+    float *mlw = reinterpret_cast<float *>(smem + L.off_ml);  // m[NC][GMAX], l[NC][GMAX]
+    pdl_wait();  // q is the preceding grid's output
+    if (ct == 0) {
+        const uint32_t qbytes = static_cast<uint32_t>(G) * HD * 4;
+        mbar_arrive_expect_tx(qbar, qbytes);
+        bulk_g2s(qs, a.q + (static_cast<size_t>(b) * a.H + static_cast<size_t>(g) * G) * HD, qbytes, qbar);
+    }
+    for (int idx = G * HD + ct; idx < GT * HD; idx += 32 * AT_CONSUMERS) qs[idx] = 0.0f;
+    if (!mbar_wait(qbar, 0)) flag_error(a.status, FLAG_TIMEOUT);
+    consumers_sync();
+
+    const float scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    const float4 *q4 = reinterpret_cast<const float4 *>(qs);
+    const int slice = lane & 7, rl = lane >> 3;
+    float mrun = -INFINITY, lrun = 0.0f;  // head `slice`
+    float2 acc[GT][DPL / 2 > 0 ? DPL / 2 : 1];
+    float accs[GT][DPL % 2 ? DPL : 1];  // unpacked accumulators when DPL is odd
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+#pragma unroll
+        for (int e = 0; e < (DPL / 2 > 0 ? DPL / 2 : 1); ++e) acc[j][e] = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int e = 0; e < (DPL % 2 ? DPL : 1); ++e) accs[j][e] = 0.0f;
+    }
+
+    for (int t = cw; t < ntiles; t += AT_CONSUMERS) {
+        const int st = t % NST;
+        if (!mbar_wait(&full[st], (t / NST) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+        const float *Kt = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
+        const float *Vt = Kt + AT_TILE * HD;
+        const int n = min(AT_TILE, t1 - (t0 + t * AT_TILE));
+
+        // ---- scores
+        float v[8][4];
+        {
+            float2 sp[GT][4];
+#pragma unroll
+            for (int j = 0; j < GT; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sp[j][k] = make_float2(0.0f, 0.0f);
+            const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
+#pragma unroll
+            for (int c = 0; c < DPL; ++c) {
+                float4 kk[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) kk[k] = K4[(rl + 4 * k) * HD4 + slice + 8 * c];
+#pragma unroll
+                for (int j = 0; j < GT; ++j) {
+                    const float4 qv = q4[j * HD4 + slice + 8 * c];
+                    const float2 qa = make_float2(qv.x, qv.y), qb = make_float2(qv.z, qv.w);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        sp[j][k] = __ffma2_rn(qa, make_float2(kk[k].x, kk[k].y), sp[j][k]);
+                        sp[j][k] = __ffma2_rn(qb, make_float2(kk[k].z, kk[k].w), sp[j][k]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[j][k] = (j < GT) ? sp[j < GT ? j : 0][k].x + sp[j < GT ? j : 0][k].y : 0.0f;
+        }
+        float my[4];
+        reduce_scatter_heads(v, slice, my);
+        const bool live = slice < G;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) my[k] = (live && rl + 4 * k < n) ? my[k] * scale2 : -INFINITY;
+        float tmax = fmaxf(fmaxf(my[0], my[1]), fmaxf(my[2], my[3]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+        const float mnew = fmaxf(mrun, tmax);
+        const float alpha = (mrun == -INFINITY) ? 0.0f : exp2f(mrun - mnew);
+        float psum = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float p = (my[k] == -INFINITY) ? 0.0f : exp2f(my[k] - mnew);
+            if (2 * slice < PR) *reinterpret_cast<float2 *>(Pw + (rl + 4 * k) * PR + 2 * slice) = make_float2(p, p);
+            psum += p;
+        }
+        psum += __shfl_xor_sync(0xffffffffu, psum, 8);
+        psum += __shfl_xor_sync(0xffffffffu, psum, 16);
+        if (live) {
+            lrun = lrun * alpha + psum;
+            mrun = mnew;
+        }
+        if (rl == 0 && slice < GT) alw[slice] = live ? alpha : 0.0f;
+        __syncwarp();
+
+        // ---- acc = alpha * acc + P V
+#pragma unroll
+        for (int j = 0; j < GT; ++j) {
+            const float al = alw[j];
+            if constexpr (DPL % 2 == 0) {
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[j][e] = __fmul2_rn(acc[j][e], make_float2(al, al));
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) accs[j][e] *= al;
+            }
+        }
+        auto row = [&](int r) {
+            float2 pp[GT];
+#pragma unroll
+            for (int j = 0; j < GT; j += 2) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(Pw + r * PR + 2 * j);
+                pp[j] = make_float2(t4.x, t4.y);
+                if (j + 1 < GT) pp[j + 1] = make_float2(t4.z, t4.w);
+            }
+            if constexpr (DPL % 2 == 0) {
+                float2 vv[DPL / 2];
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    const float *src = Vt + r * HD + VEC * (lane + 32 * u);
+                    if constexpr (VEC == 4) {
+                        const float4 tv = *reinterpret_cast<const float4 *>(src);
+                        vv[2 * u] = make_float2(tv.x, tv.y);
+                        vv[2 * u + 1] = make_float2(tv.z, tv.w);
+                    } else {
+                        vv[u] = *reinterpret_cast<const float2 *>(src);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < GT; ++j)
+#pragma unroll
+                    for (int e = 0; e < DPL / 2; ++e) acc[j][e] = __ffma2_rn(pp[j], vv[e], acc[j][e]);
+            } else {
+                float vv[DPL];
+#pragma unroll
+                for (int u = 0; u < DPL; ++u) vv[u] = Vt[r * HD + lane + 32 * u];
+#pragma unroll
+                for (int j = 0; j < GT; ++j)
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) accs[j][e] = fmaf(pp[j].x, vv[e], accs[j][e]);
+            }
+        };
+        if (n == AT_TILE) {
+#pragma unroll
+            for (int r = 0; r < AT_TILE; ++r) row(r);
+        } else {
+            for (int r = 0; r < n; ++r) row(r);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    // ---- merge the consumer warps' states
+    if (rl == 0 && slice < G) {
+        mlw[cw * GMAX + slice] = mrun;
+        mlw[(AT_CONSUMERS + cw) * GMAX + slice] = lrun;
+    }
+    consumers_sync();  // every tile consumed: the ring is idle
+    float *accw = stage;  // [NC][G][HD]
+#pragma unroll
+    for (int j = 0; j < GT; ++j) {
+        if (j < G) {
+            float *dst = accw + (cw * G + j) * HD;
+            if constexpr (DPL % 2 == 0) {
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    if constexpr (VEC == 4) {
+                        *reinterpret_cast<float4 *>(dst + 4 * (lane + 32 * u)) =
+                            make_float4(acc[j][2 * u].x, acc[j][2 * u].y, acc[j][2 * u + 1].x, acc[j][2 * u + 1].y);
+                    } else {
+                        *reinterpret_cast<float2 *>(dst + 2 * (lane + 32 * u)) = acc[j][u];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) dst[lane + 32 * e] = accs[j][e];
+            }
+        }
+    }
+    consumers_sync();
+    for (int idx = ct; idx < G * HD; idx += 32 * AT_CONSUMERS) {
+        const int j = idx / HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < AT_CONSUMERS; ++w) M = fmaxf(M, mlw[w * GMAX + j]);
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < AT_CONSUMERS; ++w) {
+            const float mw = mlw[w * GMAX + j];
+            if (mw != -INFINITY) t = fmaf(exp2f(mw - M), accw[(w * G + j) * HD + (idx - j * HD)], t);
+        }
+        rec[2 * G + idx] = t;
+        if (idx - j * HD == 0) {
+            float Ls = 0.0f;
+#pragma unroll
+            for (int w = 0; w < AT_CONSUMERS; ++w) {
+                const float mw = mlw[w * GMAX + j];
+                if (mw != -INFINITY) Ls = fmaf(exp2f(mw - M), mlw[(AT_CONSUMERS + w) * GMAX + j], Ls);
+            }
+            rec[j] = M;
+            rec[G + j] = Ls;
+        }
+    }
+}
+
+// Merge of the S partial records of one query head, for one 32-wide slice of
+// its dims (= one Q8_0 block of the output).  Each warp loads its splits'
+// records in one round, merges them locally, then warp 0 merges the warps.
+template <int DPL>
+__global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
+    constexpr int HD = 32 * DPL;
+    constexpr int NW = 8;
+    constexpr int U = 8;  // splits per warp per round
+    __shared__ float ared[NW][32];
+    __shared__ float mred[NW], lred[NW];
+    const int h = blockIdx.x, blk = blockIdx.y, b = blockIdx.z;
+    const int G = a.H / a.KV;
+    const int g = h / G, j = h - g * G;
+    const int S = a.splits;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (a.d_pos) {
+        const int pos = a.d_pos[b];
+        if (pos < 0 || pos >= a.C) {
+            pdl_wait();
+            return;
+        }
+    }
+    pdl_trigger();
+    pdl_wait();
+    const size_t ps = part_stride(G, HD);
+    const float *base = a.part + (static_cast<size_t>(b) * a.KV + g) * S * ps;
+    float Mw = -INFINITY, acc = 0.0f, Ls = 0.0f;
+    for (int s0 = warp; s0 < S; s0 += NW * U) {
+        float mv[U], lv[U], av[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int s = s0 + NW * u;
+            const bool ok = s < S;
+            const float *r = base + static_cast<size_t>(ok ? s : 0) * ps;
+            mv[u] = ok ? r[j] : -INFINITY;
+            lv[u] = ok ? r[G + j] : 0.0f;
+            av[u] = ok ? r[2 * G + j * HD + blk * 32 + lane] : 0.0f;
+        }
+        float mloc = Mw;
+#pragma unroll
+        for (int u = 0; u < U; ++u) mloc = fmaxf(mloc, mv[u]);
+        if (mloc != -INFINITY) {
+            const float sc = (Mw == -INFINITY) ? 0.0f : exp2f(Mw - mloc);
+            acc *= sc;
+            Ls *= sc;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool live = mv[u] != -INFINITY;
+                const float w = live ? exp2f(mv[u] - mloc) : 0.0f;
+                Ls = fmaf(w, live ? lv[u] : 0.0f, Ls);
+                acc = fmaf(w, live ? av[u] : 0.0f, acc);
+            }
+            Mw = mloc;
+        }
+    }
+    ared[warp][lane] = acc;
+    if (lane == 0) {
+        mred[warp] = Mw;
+        lred[warp] = Ls;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, mred[w]);
+        float t = 0.0f, L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (mred[w] != -INFINITY) {
+                const float sc = exp2f(mred[w] - M);
+                t = fmaf(sc, ared[w][lane], t);
+                L = fmaf(sc, lred[w], L);
+            }
+        }
+        const float o = __fdiv_rn(t, L);
+        a.out[(static_cast<size_t>(b) * a.H + h) * HD + blk * 32 + lane] = o;
+        if (a.out_q8) {
+            uint32_t dbits;
+            float dq;
+            const int q = q8_code(o, dbits, dq);
+            uint8_t *qb = a.out_q8 + ((static_cast<size_t>(b) * a.H + h) * (HD / 32) + blk) * Q8B;
+            qb[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+            if (lane == 0) {
+                qb[0] = static_cast<uint8_t>(dbits & 0xFF);
+                qb[1] = static_cast<uint8_t>(dbits >> 8);
+            }
+        }
+    }
+}
+
+template <int DPL, int GT>
+static int launch_attn_gt(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
+    AttnArgs a = a0;
+    const AttnSmem L = attn_smem(32 * DPL);
+    const void *fs = reinterpret_cast<const void *>(k_attn_split<DPL, GT>);
+    ensure_smem(fs, L.total);
+    void *args1[] = {&a};
+    cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(AT_THREADS), L.total, s, pdl_first, args1);
+    if (e != cudaSuccess) return -5;
+    void *args2[] = {&a};
+    e = launch(reinterpret_cast<const void *>(k_attn_combine<DPL>), dim3(a.H, DPL, B), dim3(256), 0, s, pdl_combine,
+               args2);
+    return e == cudaSuccess ? 0 : -5;
+}
+
+// Query groups of 1, 2, 4, 7 and 8 heads run exact kernels; 3, 5 and 6 run
+// in the next larger one with the extra heads masked.
+template <int DPL>
+int launch_attention_dpl(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
+    switch (a.H / a.KV) {
+        case 1: return launch_attn_gt<DPL, 1>(a, B, s, pdl_first, pdl_combine);
+        case 2: return launch_attn_gt<DPL, 2>(a, B, s, pdl_first, pdl_combine);
+        case 3:
+        case 4: return launch_attn_gt<DPL, 4>(a, B, s, pdl_first, pdl_combine);
+        case 5:
+        case 6:
+        case 7: return launch_attn_gt<DPL, 7>(a, B, s, pdl_first, pdl_combine);
+        case 8: return launch_attn_gt<DPL, 8>(a, B, s, pdl_first, pdl_combine);
+        default: return -1;
+    }
+}
+
+}  // namespace ck

@@ -316,6 +316,36 @@ def test_layer_decode_sequence_graph_devpos(dev):
     assert np.array_equal(H(g.out), o_graph) and np.array_equal(H(g.kc), k_graph)
 
 
+def test_chained_steps_in_one_graph_match_eager(dev):
+    """Several 7B-shaped steps over independent copies captured in one graph,
+    so each step's kernels launch early behind the previous step's.  Every
+    attention CTA here streams more tiles than its ring has stages.  The
+    replays must finish with a clean device status and equal the eager
+    results bit for bit."""
+    w, L, cos, sin = _layer_inputs("7b8k")
+    copies = [GpuLayer(dev, w, L, cos, sin) for _ in range(3)]
+    for g in copies:
+        g.run(w.pos)
+    torch.cuda.synchronize()
+    eager = [H(g.out).copy() for g in copies]
+    q.ck_device_status()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for g in copies:
+            ok(q.ck_decode_layer(*g.args(), w.pos, w.D, w.H, w.KV, w.hd, w.capacity, w.eps, g.scratch, g.nbytes, s))
+    for g in copies:
+        g.out.zero_()
+    for _ in range(30):
+        graph.replay()
+    torch.cuda.synchronize()
+    rc, st = q.ck_device_status()
+    assert rc == q.CK_OK and st == q.CK_OK, st
+    for g, e in zip(copies, eager):
+        assert np.array_equal(H(g.out), e)
+
+
 def test_layer_devpos_out_of_range_writes_nothing(dev):
     w, L, cos, sin = _layer_inputs("tiny")
     g = GpuLayer(dev, w, L, cos, sin)
