@@ -1,10 +1,10 @@
 // C ABI of libck_decode (declared in include/ck_decode.h): argument
 // validation on the host, launch planning, and the composition of the
-// decode step of the page "mega_fused_attention_decode_q5_0.c" as four
+// decode step of the page "mega_fused_attention_decode_q5_0.c" as five
 // kernels on one stream:
 //
-//   k_qkv          RMSNorm + Q8_0 quant (prologue), Q|K|V GEMV, bias, RoPE,
-//                  KV-cache store, q                                 STEP 1-6
+//   k_norm_q8      RMSNorm + Q8_0 quantization of the input (one CTA) STEP 1-2
+//   k_qkv_w        Q|K|V GEMV, bias, RoPE, KV-cache store, q         STEP 2-6
 //   k_attn_split   split-KV GQA-packed flash decoding                STEP 7
 //   k_attn_combine LSE merge + Q8_0 quant of the attention output    STEP 7-8
 //   k_oproj        O GEMV + bias + residual                          STEP 8
@@ -181,7 +181,7 @@ int layer_common(float *out, const float *x, const float *residual, const void *
     qa.rope_cos = rope_cos;
     qa.rope_sin = rope_sin;
     qa.q_out = reinterpret_cast<float *>(sc + L.off_q);
-    qa.xq8_out = sc + L.off_xq8;
+    qa.xq8 = sc + L.off_xq8;
     qa.d_pos = d_pos;
     qa.pos = pos;
     qa.D = D;
@@ -191,7 +191,7 @@ int layer_common(float *out, const float *x, const float *residual, const void *
     qa.C = C;
     qa.eps = eps;
     qa.status = st;
-    plan_qkv(qa);
+    if ((rc = launch_norm_q8(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
     if ((rc = launch_qkv(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
 
     AttnArgs aa{};

@@ -42,8 +42,8 @@ size_t attn_part_bytes(int B, int H, int KV, int hd, int splits) {
 }
 
 int attn_splits(int B, int KV, int max_tokens) {
-    const int nsm = device_info().num_sms;  // one CTA per SM
-    int S = (nsm + B * KV - 1) / (B * KV);
+    const int ctas = device_info().num_sms;  // one CTA per SM
+    int S = (ctas + B * KV - 1) / (B * KV);
     const int tiles = (max_tokens + AT_TILE - 1) / AT_TILE;
     if (S > tiles) S = tiles;
     if (S < 1) S = 1;

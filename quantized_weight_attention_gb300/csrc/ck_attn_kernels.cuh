@@ -7,8 +7,8 @@
 //                   One CTA owns rows [t0, t1) of one KV head and all G =
 //                   H/KV query heads that read it ("GQA-packed": each cache
 //                   row is read once per KV head).  A producer warp streams
-//                   16-row K and V tiles into a shared-memory ring through
-//                   the bulk-copy engine, keeping AT_LOOKAHEAD tiles in
+//                   8-row K and V tiles into a shared-memory ring through
+//                   the bulk-copy engine, keeping at_lookahead() tiles in
 //                   flight (refilled as tiles arrive, so they arrive one
 //                   after another instead of all at the end); six consumer
 //                   warps take tiles round-robin, each with its own online
@@ -26,13 +26,13 @@
 
 namespace ck {
 
-constexpr int AT_TILE = 16;                          // cache rows per stage
+constexpr int AT_TILE = 8;                           // cache rows per stage
+constexpr int AT_RPL = AT_TILE / 4;                  // score rows per lane
 constexpr int AT_CONSUMERS = 6;                      // consumer warps per CTA
 constexpr int AT_THREADS = 32 * (AT_CONSUMERS + 1);  // + one producer warp
-constexpr int AT_LOOKAHEAD = 5;                      // tiles in flight per CTA
 constexpr int GMAX = 8;                              // query heads per KV head
 
-// Stage count: as many 16-row K+V stages as fit in 192 KB (at most 18),
+// Stage count: as many 8-row K+V stages as fit in 192 KB (at most 18),
 // rounded down to a multiple of AT_CONSUMERS.  Tile t lives in stage
 // t % NST and is consumed by warp t % AT_CONSUMERS; with NST a multiple of
 // AT_CONSUMERS, the warp that waits for tile t on its stage's full barrier
@@ -43,8 +43,16 @@ __host__ __device__ constexpr int at_stages(int hd) {
     return ((192 * 1024) / at_stage_bytes(hd) > 18 ? 18 : (192 * 1024) / at_stage_bytes(hd)) / AT_CONSUMERS *
            AT_CONSUMERS;
 }
+// Tiles in flight per CTA: about 80 KB, so that the whole GPU keeps ~12 MB
+// of requests outstanding (enough to saturate HBM) while tiles still arrive
+// one after another instead of all at once.
+__host__ __device__ constexpr int at_lookahead(int hd) {
+    return (80 * 1024) / at_stage_bytes(hd) < 4 ? 4
+           : (80 * 1024) / at_stage_bytes(hd) > at_stages(hd) - 2 ? at_stages(hd) - 2
+                                                                   : (80 * 1024) / at_stage_bytes(hd);
+}
 static_assert(at_stages(32) % AT_CONSUMERS == 0 && at_stages(256) >= AT_CONSUMERS, "stage ring");
-static_assert(AT_LOOKAHEAD <= at_stages(256), "look-ahead exceeds the ring");
+static_assert(at_lookahead(256) < at_stages(256) && at_lookahead(32) < at_stages(32), "look-ahead exceeds the ring");
 // P row stride (floats): G heads, each duplicated into a pair, padded so
 // rows stay 16-byte aligned.
 __host__ __device__ constexpr int at_prow(int G) { return 2 * ((G + 1) & ~1); }
@@ -86,31 +94,32 @@ __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_CONSUMERS) : "memory");
 }
 
-// Reduce-scatter of v[8][4] (8 head slots x 4 rows) over the 8 lanes that
-// share a row-lane (xor 4, 2, 1): afterwards lane `slice` holds, in r[4],
-// the full sums of head `slice` for its 4 rows.
-__device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][4], int slice, float (&r)[4]) {
-    float w[4][4];
+// Reduce-scatter of v[8][R] (8 head slots x R rows) over the 8 lanes that
+// share a row-lane (xor 4, 2, 1): afterwards lane `slice` holds, in r[R],
+// the full sums of head `slice` for its R rows.
+template <int R>
+__device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][R], int slice, float (&r)[R]) {
+    float w[4][R];
     const bool b2 = slice & 4, b1 = slice & 2, b0 = slice & 1;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < R; ++k) {
             const float send = b2 ? v[j][k] : v[j + 4][k];
             const float keep = b2 ? v[j + 4][k] : v[j][k];
             w[j][k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
         }
-    float x[2][4];
+    float x[2][R];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < R; ++k) {
             const float send = b1 ? w[j][k] : w[j + 2][k];
             const float keep = b1 ? w[j + 2][k] : w[j][k];
             x[j][k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
         }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < R; ++k) {
         const float send = b0 ? x[0][k] : x[1][k];
         const float keep = b0 ? x[1][k] : x[0][k];
         r[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
@@ -123,9 +132,10 @@ __device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][4], int slice
 // Scores: lane = (slice = lane & 7, row-lane rl = lane >> 3).  A slice is
 // the float4 chunks {slice + 8c} of a row (interleaved so the 8 slices hit
 // 8 different bank groups); a lane accumulates 4 rows (rl + 4k) x GT heads
-// over its slice with packed fp32x2 FMAs (even / odd dims), then a
-// reduce-scatter over the 8 slices leaves lane (slice = j, rl) with query
-// head j's scores, and that lane owns head j's softmax state.
+// over its slice with packed fp32x2 FMAs (even / odd dims), in two passes
+// of 2 rows to bound registers; a reduce-scatter over the 8 slices leaves
+// lane (slice = j, rl) with query head j's scores, and that lane owns head
+// j's softmax state.
 // PV: lane = dims; each row adds p_j * v to GT accumulators, two dims per
 // packed FMA.
 template <int DPL, int GT>
@@ -133,6 +143,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     constexpr int HD = 32 * DPL;
     constexpr int HD4 = HD / 4;
     constexpr int NST = at_stages(HD);
+    constexpr int LA = at_lookahead(HD);
     constexpr int VEC = (DPL % 4 == 0) ? 4 : ((DPL % 2 == 0) ? 2 : 1);
     constexpr int NV = DPL / VEC;
     constexpr int PR = at_prow(GT);
@@ -207,13 +218,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         // ---- producer.  Rows before T-1 are never written by the preceding
         // grid, so they stream before waiting on it; the tile holding row
         // T-1 (the row just stored) waits first.  Tile t is issued once tile
-        // t - AT_LOOKAHEAD has arrived and its stage is free.
+        // t - LA has arrived and its stage is free.
         if (lane == 0) {
             bool ok = true;
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int st = t % NST;
-                if (t >= AT_LOOKAHEAD) {
-                    const int u = t - AT_LOOKAHEAD;
+                if (t >= LA) {
+                    const int u = t - LA;
                     ok = mbar_wait(&full[u % NST], (u / NST) & 1);
                 }
                 if (ok && t >= NST) ok = mbar_wait(&empty[st], ((t / NST) - 1) & 1);
@@ -271,49 +282,56 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         const float *Vt = Kt + AT_TILE * HD;
         const int n = min(AT_TILE, t1 - (t0 + t * AT_TILE));
 
-        // ---- scores
-        float v[8][4];
-        {
-            float2 sp[GT][4];
+        // ---- scores, rows rl + 4k, in passes of k = {2p, 2p + 1}
+        float my[AT_RPL];
+        const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
+#pragma unroll
+        for (int pass = 0; pass < AT_RPL / 2; ++pass) {
+            float2 sp[GT][2];
 #pragma unroll
             for (int j = 0; j < GT; ++j)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) sp[j][k] = make_float2(0.0f, 0.0f);
-            const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
+                for (int k = 0; k < 2; ++k) sp[j][k] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int c = 0; c < DPL; ++c) {
-                float4 kk[4];
+                float4 kk[2];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) kk[k] = K4[(rl + 4 * k) * HD4 + slice + 8 * c];
+                for (int k = 0; k < 2; ++k) kk[k] = K4[(rl + 4 * (2 * pass + k)) * HD4 + slice + 8 * c];
 #pragma unroll
                 for (int j = 0; j < GT; ++j) {
                     const float4 qv = q4[j * HD4 + slice + 8 * c];
                     const float2 qa = make_float2(qv.x, qv.y), qb = make_float2(qv.z, qv.w);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < 2; ++k) {
                         sp[j][k] = __ffma2_rn(qa, make_float2(kk[k].x, kk[k].y), sp[j][k]);
                         sp[j][k] = __ffma2_rn(qb, make_float2(kk[k].z, kk[k].w), sp[j][k]);
                     }
                 }
             }
+            float v[8][2];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[j][k] = (j < GT) ? sp[j < GT ? j : 0][k].x + sp[j < GT ? j : 0][k].y : 0.0f;
+                for (int k = 0; k < 2; ++k)
+                    v[j][k] = (j < GT) ? sp[j < GT ? j : 0][k].x + sp[j < GT ? j : 0][k].y : 0.0f;
+            float r2[2];
+            reduce_scatter_heads<2>(v, slice, r2);
+            my[2 * pass] = r2[0];
+            my[2 * pass + 1] = r2[1];
         }
-        float my[4];
-        reduce_scatter_heads(v, slice, my);
         const bool live = slice < G;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) my[k] = (live && rl + 4 * k < n) ? my[k] * scale2 : -INFINITY;
-        float tmax = fmaxf(fmaxf(my[0], my[1]), fmaxf(my[2], my[3]));
+        for (int k = 0; k < AT_RPL; ++k) my[k] = (live && rl + 4 * k < n) ? my[k] * scale2 : -INFINITY;
+        float tmax = my[0];
+#pragma unroll
+        for (int k = 1; k < AT_RPL; ++k) tmax = fmaxf(tmax, my[k]);
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 8));
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
         const float mnew = fmaxf(mrun, tmax);
         const float alpha = (mrun == -INFINITY) ? 0.0f : exp2f(mrun - mnew);
         float psum = 0.0f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < AT_RPL; ++k) {
             const float p = (my[k] == -INFINITY) ? 0.0f : exp2f(my[k] - mnew);
             if (2 * slice < PR) *reinterpret_cast<float2 *>(Pw + (rl + 4 * k) * PR + 2 * slice) = make_float2(p, p);
             psum += p;

@@ -99,37 +99,30 @@ __device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x, uint32_t
             x.sum[b] = sum;
         }
     }
+    __syncthreads();  // the row is complete before any warp reads it
 }
 
-// RMSNorm (rmsnorm_forward, T = 1) followed by Q8_0 quantization, into an
-// XRow.  sum(x^2) is carried as an unevaluated fp32 pair (two-sum plus the
-// exact FMA residual of each square), so it equals the double-precision sum
-// to ~2^-46 relative; rstd = 1/sqrt(mean + eps) is then formed in double
-// and rounded once to fp32, and y = (x * rstd) * gamma in fp32.
-//
-// Thread (warp w, lane l) owns element l of blocks w + nw*k.  With at most
-// PB blocks per warp (D <= 32*nw*PB) x and gamma are loaded once, all loads
-// in flight together, and kept in registers for the quantization pass.
-__device__ void xrow_rmsnorm_q8(const float *x, const float *gamma, float eps, int D, const XRow &xr, float *red,
-                                uint8_t *xq8_out) {
+// rstd of RMSNorm (rmsnorm_forward, T = 1) over x[0..D), for every thread
+// of the CTA.  sum(x^2) is carried as an unevaluated fp32 pair (two-sum plus
+// the exact FMA residual of each square), so it equals the double-precision
+// sum to ~2^-46 relative; rstd = 1/sqrt(mean + eps) is then formed in double
+// and rounded once to fp32.  All loads of x are issued before any is used.
+// `red` holds 2*warps + 1 floats.
+__device__ float block_rstd(const float *x, int D, float eps, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nb = D / QK;
-    constexpr int PB = 8;
-    const bool keep = nb <= nw * PB;
-    float xv[PB], gv[PB];
+    constexpr int PE = 8;
     float s = 0.0f, c = 0.0f;
-    for (int r0 = 0; r0 < nb; r0 += nw * PB) {
+    for (int i0 = 0; i0 < D; i0 += PE * static_cast<int>(blockDim.x)) {
+        float v[PE];
 #pragma unroll
-        for (int k = 0; k < PB; ++k) {
-            const int b = r0 + warp + nw * k;
-            xv[k] = b < nb ? x[b * QK + lane] : 0.0f;
-            gv[k] = (keep && b < nb) ? gamma[b * QK + lane] : 0.0f;
+        for (int k = 0; k < PE; ++k) {
+            const int i = i0 + k * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            v[k] = i < D ? x[i] : 0.0f;
         }
 #pragma unroll
-        for (int k = 0; k < PB; ++k) {
-            const float v = xv[k];
-            const float p = __fmul_rn(v, v);
-            const float e = fmaf(v, v, -p);
+        for (int k = 0; k < PE; ++k) {
+            const float p = __fmul_rn(v[k], v[k]);
+            const float e = fmaf(v[k], v[k], -p);
             float t, err;
             two_sum(s, p, t, err);
             s = t;
@@ -164,45 +157,11 @@ __device__ void xrow_rmsnorm_q8(const float *x, const float *gamma, float eps, i
         }
         if (lane == 0) {
             const double ss = static_cast<double>(s) + static_cast<double>(c);
-            red[63] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
+            red[2 * nw] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
         }
     }
     __syncthreads();
-    const float rstd = red[63];
-    for (int r0 = 0; r0 < nb; r0 += nw * PB) {
-        if (!keep) {
-#pragma unroll
-            for (int k = 0; k < PB; ++k) {
-                const int b = r0 + warp + nw * k;
-                xv[k] = b < nb ? x[b * QK + lane] : 0.0f;
-                gv[k] = b < nb ? gamma[b * QK + lane] : 0.0f;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < PB; ++k) {
-            const int b = r0 + warp + nw * k;
-            if (b < nb) {  // warp-uniform
-                const float y = __fmul_rn(__fmul_rn(xv[k], rstd), gv[k]);
-                uint32_t dbits;
-                float dq;
-                const int q = q8_code(y, dbits, dq);
-                const int sum = warp_isum(q);
-                reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
-                if (lane == 0) {
-                    xr.d[b] = dq;
-                    xr.sum[b] = sum;
-                }
-                if (xq8_out) {
-                    uint8_t *o = xq8_out + static_cast<size_t>(b) * Q8B;
-                    o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-                    if (lane == 0) {
-                        o[0] = static_cast<uint8_t>(dbits & 0xFF);
-                        o[1] = static_cast<uint8_t>(dbits >> 8);
-                    }
-                }
-            }
-        }
-    }
+    return red[2 * nw];
 }
 
 __device__ __forceinline__ XRow xrow_at(uint8_t *smem, const ProjSmem &L) {
@@ -374,11 +333,208 @@ __global__ void __launch_bounds__(256) k_block_dots(int32_t *__restrict__ isum, 
 }
 
 // ---------------------------------------------------------------------------
-// The layer's fused Q|K|V projection (STEP 1-6)
+// The layer's projections (STEP 1-6 and STEP 8)
+// ---------------------------------------------------------------------------
+// K0: RMSNorm + Q8_0 quantization of the layer input into the scratch, for
+// every projection CTA to load.  CTA c quantizes blocks [c*W, c*W + W) of the
+// W warps it has, one block per warp (y = (x * rstd) * gamma in fp32, then
+// quantize_row_q8_0); each CTA recomputes the cheap sum of squares itself.
+__global__ void __launch_bounds__(512) k_norm_q8(const QkvArgs a) {
+    __shared__ float red[64];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int pos = a.d_pos ? *a.d_pos : a.pos;
+    if (pos < 0 || pos >= a.C) {  // nothing of the step is written
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
+        pdl_wait();  // completion of this grid still implies completion of the one before
+        return;
+    }
+    pdl_trigger();
+    pdl_wait();  // x may be the previous layer's output
+    const int b = blockIdx.x * nw + warp;
+    const int nb = a.D / QK;
+    float xv = 0.0f, gv = 0.0f;
+    if (b < nb) {
+        xv = a.x[b * QK + lane];
+        gv = a.gamma[b * QK + lane];
+    }
+    const float rstd = block_rstd(a.x, a.D, a.eps, red);
+    if (b >= nb) return;  // warp-uniform
+    const float y = __fmul_rn(__fmul_rn(xv, rstd), gv);
+    uint32_t dbits;
+    float dq;
+    const int q = q8_code(y, dbits, dq);
+    uint8_t *o = a.xq8 + static_cast<size_t>(b) * Q8B;
+    o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    if (lane == 0) {
+        o[0] = static_cast<uint8_t>(dbits & 0xFF);
+        o[1] = static_cast<uint8_t>(dbits >> 8);
+    }
+}
+
+// Warp tasks.  A warp owns two weight rows: a RoPE pair (rows h*hd + i and
+// h*hd + hd/2 + i) for Q and K, two consecutive rows for V and O.  Its lane
+// 0 copies both rows into the warp's own shared-memory slot with the
+// bulk-copy engine at kernel start (before waiting on the preceding grid);
+// lanes 0-15 decode the segments of the first row and lanes 16-31 those of
+// the second, a shuffle tree sums them, and lane 0 runs the epilogue.  No
+// CTA-wide barrier follows the activation prologue.
+struct QkvTask {
+    int kind;  // 0 = Q, 1 = K, 2 = V, 3 = none
+    int ra, rb, head, i;
+};
+
+__device__ __forceinline__ QkvTask qkv_task(const QkvArgs &a, int t) {
+    QkvTask T{};
+    const int half = a.hd >> 1;
+    const int nq = a.H * half, nk = a.KV * half, nv = (a.KV * a.hd) >> 1;
+    if (t < nq) {
+        T.kind = 0;
+        T.head = t / half;
+        T.i = t - T.head * half;
+    } else if (t < nq + nk) {
+        T.kind = 1;
+        T.head = (t - nq) / half;
+        T.i = (t - nq) - T.head * half;
+    } else if (t < nq + nk + nv) {
+        T.kind = 2;
+        T.ra = 2 * (t - nq - nk);
+        T.rb = T.ra + 1;
+        return T;
+    } else {
+        T.kind = 3;
+        return T;
+    }
+    T.ra = T.head * a.hd + T.i;
+    T.rb = T.ra + half;
+    return T;
+}
+
+int qkv_tasks(const QkvArgs &a) { return (a.H + a.KV) * (a.hd >> 1) + ((a.KV * a.hd) >> 1); }
+
+// Sum over the segments [li, li + 16, ...) of one staged row, then over the
+// 16 lanes of each half-warp (lane 0: first row, lane 16: second row).
+template <bool Q8>
+__device__ __forceinline__ float warp_row_dot(const uint8_t *row, int nseg, int li, const XRow &x) {
+    float acc = 0.0f;
+    for (int k = li; k < nseg; k += 16)
+        acc += seg_dot<Q8>(reinterpret_cast<const uint4 *>(row + k * SegShape<Q8>::BYTES), x, k * 8);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    return acc;
+}
+
+__global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int nb = a.D / QK, nseg = nb / 8;
+    const int rb5 = nb * Q5B, rb8 = nb * Q8B;
+    const ProjSmem L = proj_smem(1, nb, static_cast<size_t>(nw) * 2 * rb8);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp;
+    uint8_t *slot = smem + L.off_w + static_cast<size_t>(warp) * 2 * rb8;
+    const XRow x = xrow_at(smem, L);
+    const QkvTask T = qkv_task(a, blockIdx.x * nw + warp);
+    const int pos = a.d_pos ? *a.d_pos : a.pos;
+    if (pos < 0 || pos >= a.C) {
+        pdl_wait();
+        return;
+    }
+    const bool q8 = T.kind == 2;
+    const int rb = q8 ? rb8 : rb5;
+    if (lane == 0 && T.kind != 3) {  // the weights do not depend on earlier grids
+        const uint8_t *W = T.kind == 0 ? a.wq : (T.kind == 1 ? a.wk : a.wv);
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * rb));
+        if (q8) {
+            bulk_g2s(slot, W + static_cast<size_t>(T.ra) * rb, static_cast<uint32_t>(2 * rb), bar);
+        } else {
+            bulk_g2s(slot, W + static_cast<size_t>(T.ra) * rb, static_cast<uint32_t>(rb), bar);
+            bulk_g2s(slot + rb, W + static_cast<size_t>(T.rb) * rb, static_cast<uint32_t>(rb), bar);
+        }
+    }
+    pdl_trigger();
+    pdl_wait();  // the quantized input is ready
+    xrow_from_q8(a.xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    if (T.kind == 3) return;
+    if (!mbar_wait(bar, 0)) flag_error(a.status, FLAG_TIMEOUT);
+    const uint8_t *row = slot + (lane >> 4) * rb;
+    const float acc = q8 ? warp_row_dot<true>(row, nseg, lane & 15, x) : warp_row_dot<false>(row, nseg, lane & 15, x);
+    const float sb = __shfl_sync(0xffffffffu, acc, 16);
+    if (lane != 0) return;
+    if (T.kind == 2) {
+        const float va = acc + (a.bv ? a.bv[T.ra] : 0.0f);
+        const float vb = sb + (a.bv ? a.bv[T.rb] : 0.0f);
+        int h = T.ra / a.hd;
+        a.v_cache[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.ra - h * a.hd)] = va;
+        h = T.rb / a.hd;
+        a.v_cache[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.rb - h * a.hd)] = vb;
+        return;
+    }
+    // bias, then rotate-half RoPE of the pair (i, i + hd/2) at row `pos`
+    const int half = a.hd >> 1;
+    const float *bias = T.kind == 0 ? a.bq : a.bk;
+    const float A = acc + (bias ? bias[T.ra] : 0.0f);
+    const float B = sb + (bias ? bias[T.rb] : 0.0f);
+    const float c = a.rope_cos[static_cast<size_t>(pos) * half + T.i];
+    const float s = a.rope_sin[static_cast<size_t>(pos) * half + T.i];
+    const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, s));
+    const float B2 = __fadd_rn(__fmul_rn(A, s), __fmul_rn(B, c));
+    if (T.kind == 0) {
+        a.q_out[T.ra] = A2;
+        a.q_out[T.rb] = B2;
+    } else {
+        float *kr = a.k_cache + (static_cast<size_t>(T.head) * a.C + pos) * a.hd;
+        kr[T.i] = A2;
+        kr[T.i + half] = B2;
+    }
+}
+
+__global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int nb = a.QD / QK, nseg = nb / 8;
+    const int rb = nb * Q5B;
+    const ProjSmem L = proj_smem(1, nb, static_cast<size_t>(nw) * 2 * rb);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp;
+    uint8_t *slot = smem + L.off_w + static_cast<size_t>(warp) * 2 * rb;
+    const XRow x = xrow_at(smem, L);
+    const int r0 = 2 * (blockIdx.x * nw + warp);
+    const bool valid = r0 < a.D;
+    if (a.d_pos) {
+        const int pos = *a.d_pos;
+        if (pos < 0 || pos >= a.C) {
+            pdl_wait();
+            return;
+        }
+    }
+    if (lane == 0 && valid) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * rb));
+        bulk_g2s(slot, a.wo + static_cast<size_t>(r0) * rb, static_cast<uint32_t>(2 * rb), bar);
+    }
+    pdl_trigger();
+    pdl_wait();  // the attention output is ready
+    xrow_from_q8(a.aq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    if (!valid) return;
+    if (!mbar_wait(bar, 0)) flag_error(a.status, FLAG_TIMEOUT);
+    const float acc = warp_row_dot<false>(slot + (lane >> 4) * rb, nseg, lane & 15, x);
+    const float sb = __shfl_sync(0xffffffffu, acc, 16);
+    if (lane == 0) {
+        a.out[r0] = (acc + (a.bo ? a.bo[r0] : 0.0f)) + a.residual[r0];
+        a.out[r0 + 1] = (sb + (a.bo ? a.bo[r0 + 1] : 0.0f)) + a.residual[r0 + 1];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Direct path of the layer (rows whose block count is not a multiple of 8)
 // ---------------------------------------------------------------------------
 // Tiles: Q and K tiles hold 16 RoPE pairs of one head (rows h*hd + i0 + i
 // and h*hd + hd/2 + i0 + i, i < 16), so the epilogue rotates without a
-// second pass; V tiles hold rv consecutive rows.
+// second pass; V tiles hold rv consecutive rows.  A warp per row, a lane per
+// block, aligned 32-bit global loads that never leave the block.
 struct QkvTile {
     int kind;  // 0 = Q, 1 = K, 2 = V
     int head, i0, v0, rows;
@@ -406,64 +562,32 @@ __device__ __forceinline__ QkvTile qkv_tile(const QkvArgs &a, int t) {
     return T;
 }
 
-__host__ __device__ inline size_t qkv_wbytes(int nb, int rv) {
-    const size_t a = 32u * static_cast<size_t>(row_stride(nb, false));
-    const size_t b = static_cast<size_t>(rv) * row_stride(nb, true);
-    return a > b ? a : b;
-}
-
-template <bool FAST>
-__global__ void __launch_bounds__(512, 1) k_qkv(const QkvArgs a) {
+__global__ void __launch_bounds__(256) k_qkv_direct(const QkvArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const QkvTile T = qkv_tile(a, blockIdx.x);
     const int half = a.hd >> 1;
-    const int nb = a.D / QK, nseg = nb / 8;
+    const int nb = a.D / QK;
     const bool q8 = T.kind == 2;
     const uint8_t *W = T.kind == 0 ? a.wq : (T.kind == 1 ? a.wk : a.wv);
-    const int rb = nb * (q8 ? Q8B : Q5B);
-    const int rstride = row_stride(nb, q8);
-    const int Rmax = max(32, a.rv);
-    const ProjSmem L = proj_smem(Rmax, nb, FAST ? qkv_wbytes(nb, a.rv) : 0);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint8_t *wsm = smem + L.off_w;
-    float *part = reinterpret_cast<float *>(smem + L.off_part);
+    const ProjSmem L = proj_smem(max(32, a.rv), nb, 0);
     float *rowsum = reinterpret_cast<float *>(smem + L.off_rowsum);
-    float *red = reinterpret_cast<float *>(smem + L.off_red);
     const XRow x = xrow_at(smem, L);
     auto rowof = [&](int i) {
         return T.kind == 2 ? T.v0 + i : T.head * a.hd + (i < 16 ? T.i0 + i : half + T.i0 + i - 16);
     };
-
     const int pos = a.d_pos ? *a.d_pos : a.pos;
-    if (pos < 0 || pos >= a.C) {  // uniform over the grid: nothing is written
-        if (blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
-        pdl_wait();  // completion of this grid must still imply completion of the one before
+    if (pos < 0 || pos >= a.C) {
+        pdl_wait();
         return;
     }
-    if constexpr (FAST) {
-        init_bars(bars, (T.rows + 15) >> 4);
-        __syncthreads();
-        issue_rows(wsm, rstride, W, rb, T.rows, bars, rowof);  // weights do not depend on earlier grids
-    }
     pdl_trigger();
-    pdl_wait();  // x may be the previous layer's output
-    xrow_rmsnorm_q8(a.x, a.gamma, a.eps, a.D, x, red, blockIdx.x == 0 ? a.xq8_out : nullptr);
+    pdl_wait();  // the quantized input is ready
+    xrow_from_q8(a.xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    if (q8)
+        tile_direct<true>(W, nb, T.rows, rowof, x, rowsum);
+    else
+        tile_direct<false>(W, nb, T.rows, rowof, x, rowsum);
     __syncthreads();
-    if constexpr (FAST) {
-        if (q8)
-            tile_segments<true>(wsm, rstride, T.rows, Rmax, nseg, bars, x, part, a.status);
-        else
-            tile_segments<false>(wsm, rstride, T.rows, Rmax, nseg, bars, x, part, a.status);
-        __syncthreads();
-        reduce_rows(part, Rmax, T.rows, nseg, rowsum);
-    } else {
-        if (q8)
-            tile_direct<true>(W, nb, T.rows, rowof, x, rowsum);
-        else
-            tile_direct<false>(W, nb, T.rows, rowof, x, rowsum);
-    }
-    __syncthreads();
-
     if (T.kind == 2) {
         for (int i = threadIdx.x; i < T.rows; i += blockDim.x) {
             const int r = T.v0 + i;
@@ -472,7 +596,6 @@ __global__ void __launch_bounds__(512, 1) k_qkv(const QkvArgs a) {
             a.v_cache[(static_cast<size_t>(h) * a.C + pos) * a.hd + d] = v;
         }
     } else if (threadIdx.x < 16) {
-        // bias, then rotate-half RoPE of the pair (d, d + hd/2) at row `pos`
         const int i = threadIdx.x, d = T.i0 + i;
         const int ra = rowof(i), rb2 = rowof(16 + i);
         const float *bias = T.kind == 0 ? a.bq : a.bk;
@@ -493,22 +616,13 @@ __global__ void __launch_bounds__(512, 1) k_qkv(const QkvArgs a) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// The layer's O projection + bias + residual (STEP 8)
-// ---------------------------------------------------------------------------
-template <bool FAST>
-__global__ void __launch_bounds__(512, 1) k_oproj(const OprojArgs a) {
+__global__ void __launch_bounds__(256) k_oproj_direct(const OprojArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int nb = a.QD / QK, nseg = nb / 8;
-    const int rb = nb * Q5B;
-    const int rstride = row_stride(nb, false);
+    const int nb = a.QD / QK;
     const int R = a.rows_per_cta;
     const int r0 = blockIdx.x * R;
     const int rows = min(R, a.D - r0);
-    const ProjSmem L = proj_smem(R, nb, FAST ? static_cast<size_t>(R) * rstride : 0);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
-    uint8_t *wsm = smem + L.off_w;
-    float *part = reinterpret_cast<float *>(smem + L.off_part);
+    const ProjSmem L = proj_smem(R, nb, 0);
     float *rowsum = reinterpret_cast<float *>(smem + L.off_rowsum);
     const XRow x = xrow_at(smem, L);
     auto rowof = [r0](int i) { return r0 + i; };
@@ -519,27 +633,14 @@ __global__ void __launch_bounds__(512, 1) k_oproj(const OprojArgs a) {
             return;
         }
     }
-    if constexpr (FAST) {
-        init_bars(bars, (rows + 15) >> 4);
-        __syncthreads();
-        issue_rows(wsm, rstride, a.wo, rb, rows, bars, rowof);
-    }
     pdl_trigger();
     pdl_wait();  // the attention output is ready
     xrow_from_q8(a.aq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
-    __syncthreads();
-    if constexpr (FAST) {
-        tile_segments<false>(wsm, rstride, rows, R, nseg, bars, x, part, a.status);
-        __syncthreads();
-        reduce_rows(part, R, rows, nseg, rowsum);
-    } else {
-        tile_direct<false>(a.wo, nb, rows, rowof, x, rowsum);
-    }
+    tile_direct<false>(a.wo, nb, rows, rowof, x, rowsum);
     __syncthreads();
     for (int i = threadIdx.x; i < rows; i += blockDim.x) {
         const int r = r0 + i;
-        const float o = rowsum[i] + (a.bo ? a.bo[r] : 0.0f);
-        a.out[r] = o + a.residual[r];
+        a.out[r] = (rowsum[i] + (a.bo ? a.bo[r] : 0.0f)) + a.residual[r];
     }
 }
 
@@ -634,46 +735,63 @@ void plan_qkv(QkvArgs &a) {
     a.rv = rv;
 }
 
-static bool qkv_fast(const QkvArgs &a, size_t *smem_total) {
-    const int nb = a.D / QK;
-    const bool fast = nb % 8 == 0;
-    const ProjSmem L = proj_smem(a.rv > 32 ? a.rv : 32, nb, fast ? qkv_wbytes(nb, a.rv) : 0);
-    *smem_total = L.total;
-    return fast;
+// Warps per CTA of a warp-task GEMV whose slots hold two rows of `rb` bytes:
+// 16, fewer when the slots would not fit in shared memory, 0 if one does not.
+static int task_warps(int nb, int rb) {
+    const size_t other = proj_smem(1, nb, 0).total;
+    const size_t avail = device_info().smem_optin;
+    int w = 16;
+    while (w > 0 && other + static_cast<size_t>(w) * 2 * rb > avail) w >>= 1;
+    return w;
 }
 
-int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl) {
-    size_t smem;
-    const bool fast = qkv_fast(a, &smem);
-    if (smem > device_info().smem_optin) return -1;
+int launch_norm_q8(const QkvArgs &a0, cudaStream_t s, bool pdl) {
+    QkvArgs a = a0;
+    const int warps = 16;
+    const int grid = (a.D / QK + warps - 1) / warps;
+    void *args[] = {&a};
+    return cuda_status(launch(reinterpret_cast<const void *>(k_norm_q8), dim3(grid), dim3(32 * warps), 0, s, pdl, args));
+}
+
+int launch_qkv(const QkvArgs &a0, cudaStream_t s, bool pdl) {
+    QkvArgs a = a0;
     const int nb = a.D / QK;
-    const int v_tiles = (a.KV * a.hd + a.rv - 1) / a.rv;
-    const int grid = a.n_q_tiles + a.n_k_tiles + v_tiles;
-    const int tasks = 2 * ((nb / 8 + 1) / 2);
-    const int vt = ((a.rv + 15) / 16) * ((nb / 8 + 1) / 2);
-    int warps = fast ? (tasks > vt ? tasks : vt) : 8;
-    warps = warps < 4 ? 4 : (warps > 16 ? 16 : warps);
-    QkvArgs arg = a;
-    void *args[] = {&arg};
-    const void *fn = fast ? reinterpret_cast<const void *>(k_qkv<true>) : reinterpret_cast<const void *>(k_qkv<false>);
+    const int warps = (nb % 8 == 0) ? task_warps(nb, nb * Q8B) : 0;
+    void *args[] = {&a};
+    if (warps > 0) {
+        const size_t smem = proj_smem(1, nb, static_cast<size_t>(warps) * 2 * nb * Q8B).total;
+        const int grid = (qkv_tasks(a) + warps - 1) / warps;
+        const void *fn = reinterpret_cast<const void *>(k_qkv_w);
+        ensure_smem(fn, smem);
+        return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), smem, s, pdl, args));
+    }
+    plan_qkv(a);
+    const size_t smem = proj_smem(a.rv > 32 ? a.rv : 32, nb, 0).total;
+    if (smem > device_info().smem_optin) return -1;
+    const int grid = a.n_q_tiles + a.n_k_tiles + (a.KV * a.hd + a.rv - 1) / a.rv;
+    const void *fn = reinterpret_cast<const void *>(k_qkv_direct);
     ensure_smem(fn, smem);
-    return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), smem, s, pdl, args));
+    return cuda_status(launch(fn, dim3(grid), dim3(256), smem, s, pdl, args));
 }
 
 int launch_oproj(const OprojArgs &a0, cudaStream_t s, bool pdl) {
     OprojArgs a = a0;
     const int nb = a.QD / QK;
-    const bool fast = nb % 8 == 0;
-    a.rows_per_cta = fast ? gemv_rows_per_cta(a.D, nb, false) : 8;
-    const int R = a.rows_per_cta;
-    const ProjSmem L = proj_smem(R, nb, fast ? static_cast<size_t>(R) * row_stride(nb, false) : 0);
-    const int grid = (a.D + R - 1) / R;
-    int warps = fast ? ((R + 15) / 16) * ((nb / 8 + 1) / 2) : 8;
-    warps = warps < 4 ? 4 : (warps > 16 ? 16 : warps);
+    const int warps = (nb % 8 == 0) ? task_warps(nb, nb * Q5B) : 0;
     void *args[] = {&a};
-    const void *fn = fast ? reinterpret_cast<const void *>(k_oproj<true>) : reinterpret_cast<const void *>(k_oproj<false>);
-    ensure_smem(fn, L.total);
-    return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), L.total, s, pdl, args));
+    if (warps > 0) {
+        const size_t smem = proj_smem(1, nb, static_cast<size_t>(warps) * 2 * nb * Q5B).total;
+        const int grid = (a.D / 2 + warps - 1) / warps;
+        const void *fn = reinterpret_cast<const void *>(k_oproj_w);
+        ensure_smem(fn, smem);
+        return cuda_status(launch(fn, dim3(grid), dim3(32 * warps), smem, s, pdl, args));
+    }
+    a.rows_per_cta = 8;
+    const size_t smem = proj_smem(8, nb, 0).total;
+    const int grid = (a.D + 7) / 8;
+    const void *fn = reinterpret_cast<const void *>(k_oproj_direct);
+    ensure_smem(fn, smem);
+    return cuda_status(launch(fn, dim3(grid), dim3(256), smem, s, pdl, args));
 }
 
 }  // namespace ck

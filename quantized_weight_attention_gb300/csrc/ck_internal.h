@@ -38,7 +38,7 @@ struct QkvArgs {
     float *k_cache, *v_cache;
     const float *rope_cos, *rope_sin;
     float *q_out;        // [H*hd] rotated q
-    uint8_t *xq8_out;    // [D/32] Q8_0 blocks of the normed input (written by CTA 0)
+    uint8_t *xq8;        // [D/32] Q8_0 blocks of the normed input (written by K0, read by K1)
     const int32_t *d_pos;  // device position (or null: use pos)
     int pos;
     int D, H, KV, hd, C;
@@ -56,6 +56,7 @@ struct OprojArgs {
     int D, QD, rows_per_cta, C;
     unsigned *status;
 };
+int launch_norm_q8(const QkvArgs &a, cudaStream_t s, bool pdl);
 int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl);
 int launch_oproj(const OprojArgs &a, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);
