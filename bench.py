@@ -228,8 +228,9 @@ def run_ours(args, ws, rank, local, pg):
     K, W = args.steps, max(args.warmup, 3)
     rem = K % R
     g_rem = capture(rem) if rem else None
-    for _ in range(-(-W // R)):
-        g_full.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // R)):
+            g_full.replay()
     W = -(-W // R) * R
     torch.cuda.synchronize()
 
@@ -239,12 +240,13 @@ def run_ours(args, ws, rank, local, pg):
     barrier(pg, torch)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.perf_counter()
-    ev0.record(stream)
-    for _ in range(K // R):
-        g_full.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        ev0.record(stream)
+        for _ in range(K // R):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
     ev1.synchronize()
     barrier(pg, torch)
     wall = time.perf_counter() - wall0
@@ -372,18 +374,20 @@ def run_stack(args, ws, pg, torch, q, synth, dev):
     with torch.cuda.graph(g, stream=stream):
         token()
     K, W = args.steps, max(args.warmup, 3)
-    for _ in range(W):
-        g.replay()
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            g.replay()
     torch.cuda.synchronize()
     sampler = ClockSampler(gpu_uuid(torch, dev))
     sampler.start()
     time.sleep(0.3)
     barrier(pg, torch)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(K):
-        g.replay()
-    ev1.record(stream)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        ev0.record(stream)
+        for _ in range(K):
+            g.replay()
+        ev1.record(stream)
     ev1.synchronize()
     barrier(pg, torch)
     clocks = sampler.stop()
