@@ -122,7 +122,7 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
 // Layout of the layer scratch (all offsets 256-byte aligned).
 struct LayerScratch {
-    size_t off_q, off_xq8, off_attn, off_aq8, off_part, total;
+    size_t off_q, off_xq8, off_attn, off_aq8, off_apack, off_part, total;
     int splits;
 };
 
@@ -140,6 +140,8 @@ LayerScratch layer_scratch(int D, int H, int KV, int hd, int C) {
     o = a256(o + static_cast<size_t>(H) * hd * 4);
     L.off_aq8 = o;
     o = a256(o + static_cast<size_t>(H * hd / 32) * 34);
+    L.off_apack = o;
+    o = a256(o + xpack_bytes(H * hd / 32));
     L.off_part = o;
     o = a256(o + attn_part_bytes(1, H, KV, hd, L.splits));
     L.total = o;
@@ -191,7 +193,8 @@ int layer_common(float *out, const float *x, const float *residual, const void *
     qa.C = C;
     qa.eps = eps;
     qa.status = st;
-    if ((rc = launch_norm_q8(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
+    qa.fused_norm = qkv_fused_norm_ok(qa) ? 1 : 0;
+    if (!qa.fused_norm && (rc = launch_norm_q8(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
     if ((rc = launch_qkv(qa, s, true))) return rc == -1 ? CK_EINVAL : CK_ECUDA;
 
     AttnArgs aa{};
@@ -208,6 +211,7 @@ int layer_common(float *out, const float *x, const float *residual, const void *
     aa.part = reinterpret_cast<float *>(sc + L.off_part);
     aa.out = reinterpret_cast<float *>(sc + L.off_attn);
     aa.out_q8 = sc + L.off_aq8;
+    aa.out_pack = sc + L.off_apack;
     aa.l2_prefetch = wo;
     aa.l2_prefetch_bytes = static_cast<size_t>(D) * (H * hd / 32) * 22;
     aa.status = st;
@@ -219,6 +223,7 @@ int layer_common(float *out, const float *x, const float *residual, const void *
     oa.wo = static_cast<const uint8_t *>(wo);
     oa.bo = bo;
     oa.aq8 = sc + L.off_aq8;
+    oa.apack = sc + L.off_apack;
     oa.d_pos = d_pos;
     oa.D = D;
     oa.QD = H * hd;

@@ -541,6 +541,17 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
                 qb[0] = static_cast<uint8_t>(dbits & 0xFF);
                 qb[1] = static_cast<uint8_t>(dbits >> 8);
             }
+            if (a.out_pack) {  // the same block in the packed row the O-projection copies
+                const int nbo = a.H * (HD / 32), bq = h * (HD / 32) + blk;
+                uint8_t *pk = a.out_pack + static_cast<size_t>(b) * xpack_bytes(nbo);
+                pk[static_cast<size_t>(xq_chunk(bq, lane >> 4)) * 16 + (lane & 15)] =
+                    static_cast<uint8_t>(static_cast<int8_t>(q));
+                const int sum = warp_isum(q);
+                if (lane == 0) {
+                    reinterpret_cast<float *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16)[bq] = dq;
+                    reinterpret_cast<int *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16 + nbo * 4)[bq] = sum;
+                }
+            }
         }
     }
 }

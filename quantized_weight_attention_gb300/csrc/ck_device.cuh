@@ -145,6 +145,11 @@ __device__ __forceinline__ int isum_q8_0(const uint32_t (&qs)[8], const int (&xw
 // segment columns that one warp reads at a time never conflict.
 __host__ __device__ constexpr int xq_chunk(int b, int c) { return 2 * b + c + (b >> 3); }
 __host__ __device__ constexpr int xq_chunks(int nb) { return 2 * nb + nb / 8 + 1; }
+// Bytes of a packed row: the XRow image (codes in the chunk layout, then nb
+// fp32 scales, then nb int32 code sums), rounded up to 16.
+__host__ __device__ constexpr size_t xpack_bytes(int nb) {
+    return (static_cast<size_t>(xq_chunks(nb)) * 16 + static_cast<size_t>(nb) * 8 + 15) / 16 * 16;
+}
 
 struct XRow {
     int4 *q;     // codes, layout above

@@ -102,33 +102,13 @@ __device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x, uint32_t
     __syncthreads();  // the row is complete before any warp reads it
 }
 
-// rstd of RMSNorm (rmsnorm_forward, T = 1) over x[0..D), for every thread
-// of the CTA.  sum(x^2) is carried as an unevaluated fp32 pair (two-sum plus
-// the exact FMA residual of each square), so it equals the double-precision
-// sum to ~2^-46 relative; rstd = 1/sqrt(mean + eps) is then formed in double
-// and rounded once to fp32.  All loads of x are issued before any is used.
-// `red` holds 2*warps + 1 floats.
-__device__ float block_rstd(const float *x, int D, float eps, float *red) {
+// rstd = 1/sqrt(mean + eps) from every thread's (sum, compensation) pair of
+// x^2 terms: the pairs are combined with two-sums (warp, then CTA), so the
+// total equals the double-precision sum to ~2^-46 relative; rstd is then
+// formed in double and rounded once to fp32.  `red` holds 2*warps + 1
+// floats.  Every thread of the CTA gets rstd.
+__device__ float rstd_from_pairs(float s, float c, int D, float eps, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    constexpr int PE = 8;
-    float s = 0.0f, c = 0.0f;
-    for (int i0 = 0; i0 < D; i0 += PE * static_cast<int>(blockDim.x)) {
-        float v[PE];
-#pragma unroll
-        for (int k = 0; k < PE; ++k) {
-            const int i = i0 + k * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
-            v[k] = i < D ? x[i] : 0.0f;
-        }
-#pragma unroll
-        for (int k = 0; k < PE; ++k) {
-            const float p = __fmul_rn(v[k], v[k]);
-            const float e = fmaf(v[k], v[k], -p);
-            float t, err;
-            two_sum(s, p, t, err);
-            s = t;
-            c = __fadd_rn(c, __fadd_rn(err, e));
-        }
-    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
@@ -162,6 +142,92 @@ __device__ float block_rstd(const float *x, int D, float eps, float *red) {
     }
     __syncthreads();
     return red[2 * nw];
+}
+
+// Accumulate v^2 into the unevaluated pair (s, c): two-sum of the rounded
+// square plus its exact FMA residual.
+__device__ __forceinline__ void sumsq_add(float v, float &s, float &c) {
+    const float p = __fmul_rn(v, v);
+    const float e = fmaf(v, v, -p);
+    float t, err;
+    two_sum(s, p, t, err);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(err, e));
+}
+
+// rstd of RMSNorm (rmsnorm_forward, T = 1) over x[0..D), for every thread
+// of the CTA.  All loads of x are issued before any is used.
+__device__ float block_rstd(const float *x, int D, float eps, float *red) {
+    constexpr int PE = 8;
+    float s = 0.0f, c = 0.0f;
+    for (int i0 = 0; i0 < D; i0 += PE * static_cast<int>(blockDim.x)) {
+        float v[PE];
+#pragma unroll
+        for (int k = 0; k < PE; ++k) {
+            const int i = i0 + k * static_cast<int>(blockDim.x) + static_cast<int>(threadIdx.x);
+            v[k] = i < D ? x[i] : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < PE; ++k) sumsq_add(v[k], s, c);
+    }
+    return rstd_from_pairs(s, c, D, eps, red);
+}
+
+// RMSNorm + quantize_row_q8_0 of the whole input row straight into this
+// CTA's shared-memory XRow (the projection prologue): warp w takes blocks
+// w, w + W, ... (at most NORM_XPW of them), every load of x is issued before
+// any is used, y = (x * rstd) * gamma in fp32, and the Q8_0 codes, scales and
+// code sums land in the XRow layout.  `gv` holds the warp's gamma values
+// (loaded before the wait on the preceding grid).  When `tap` is set the
+// Q8_0 blocks are also written there.
+constexpr int NORM_XPW = 8;
+__device__ void norm_quant_xrow(const float *x, const float (&gv)[NORM_XPW], int nb, int D, float eps, const XRow &xr,
+                                float *red, uint8_t *tap) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float xv[NORM_XPW];
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        const int b = warp + nw * j;
+        xv[j] = b < nb ? x[b * QK + lane] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) sumsq_add(xv[j], s, c);
+    const float rstd = rstd_from_pairs(s, c, D, eps, red);
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        const int b = warp + nw * j;
+        if (b < nb) {  // warp-uniform
+            const float y = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
+            uint32_t dbits;
+            float dq;
+            const int q = q8_code(y, dbits, dq);
+            reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
+            const int sum = warp_isum(q);
+            if (lane == 0) {
+                xr.d[b] = dq;
+                xr.sum[b] = sum;
+            }
+            if (tap) {
+                uint8_t *o = tap + static_cast<size_t>(b) * Q8B;
+                o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+                if (lane == 0) {
+                    o[0] = static_cast<uint8_t>(dbits & 0xFF);
+                    o[1] = static_cast<uint8_t>(dbits >> 8);
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// A packed activation row (the XRow image, written by its producer kernel)
+// copied into the CTA's XRow: one 16-byte load per thread.
+__device__ void xrow_from_pack(const uint8_t *pack, int nb, const XRow &xr) {
+    const int n16 = static_cast<int>(xpack_bytes(nb) / 16);
+    int4 *dst = xr.q;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = __ldcg(reinterpret_cast<const int4 *>(pack) + i);
+    __syncthreads();
 }
 
 __device__ __forceinline__ XRow xrow_at(uint8_t *smem, const ProjSmem &L) {
@@ -436,7 +502,8 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
     const XRow x = xrow_at(smem, L);
     const QkvTask T = qkv_task(a, blockIdx.x * nw + warp);
     const int pos = a.d_pos ? *a.d_pos : a.pos;
-    if (pos < 0 || pos >= a.C) {
+    if (pos < 0 || pos >= a.C) {  // nothing of the step is written
+        if (a.fused_norm && blockIdx.x == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
         pdl_wait();
         return;
     }
@@ -455,8 +522,20 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
         }
     }
     pdl_trigger();
-    pdl_wait();  // the quantized input is ready
-    xrow_from_q8(a.xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    if (a.fused_norm) {
+        float gv[NORM_XPW];  // gamma does not depend on the preceding grid
+#pragma unroll
+        for (int j = 0; j < NORM_XPW; ++j) {
+            const int b = warp + nw * j;
+            gv[j] = b < nb ? __ldg(a.gamma + b * QK + lane) : 0.0f;
+        }
+        pdl_wait();  // x may be the previous layer's output
+        norm_quant_xrow(a.x, gv, nb, a.D, a.eps, x, reinterpret_cast<float *>(smem + L.off_red),
+                        blockIdx.x == 0 ? a.xq8 : nullptr);
+    } else {
+        pdl_wait();  // the quantized input is ready
+        xrow_from_q8(a.xq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    }
     if (T.kind == 3) return;
     if (!mbar_wait(bar, 0)) flag_error(a.status, FLAG_TIMEOUT);
     const uint8_t *row = slot + (lane >> 4) * rb;
@@ -517,7 +596,10 @@ __global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
     }
     pdl_trigger();
     pdl_wait();  // the attention output is ready
-    xrow_from_q8(a.aq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
+    if (a.apack)
+        xrow_from_pack(a.apack, nb, x);
+    else
+        xrow_from_q8(a.aq8, nb, x, reinterpret_cast<uint32_t *>(smem + L.off_raw));
     if (!valid) return;
     if (!mbar_wait(bar, 0)) flag_error(a.status, FLAG_TIMEOUT);
     const float acc = warp_row_dot<false>(slot + (lane >> 4) * rb, nseg, lane & 15, x);
@@ -751,6 +833,13 @@ int launch_norm_q8(const QkvArgs &a0, cudaStream_t s, bool pdl) {
     const int grid = (a.D / QK + warps - 1) / warps;
     void *args[] = {&a};
     return cuda_status(launch(reinterpret_cast<const void *>(k_norm_q8), dim3(grid), dim3(32 * warps), 0, s, pdl, args));
+}
+
+bool qkv_fused_norm_ok(const QkvArgs &a) {
+    const int nb = a.D / QK;
+    if (nb % 8 != 0) return false;
+    const int warps = task_warps(nb, nb * Q8B);
+    return warps > 0 && warps * NORM_XPW >= nb;
 }
 
 int launch_qkv(const QkvArgs &a0, cudaStream_t s, bool pdl) {

@@ -44,6 +44,7 @@ struct QkvArgs {
     int D, H, KV, hd, C;
     float eps;
     int n_q_tiles, n_k_tiles, rv;  // Q / K tiles of 16 RoPE pairs, V tiles of rv rows
+    int fused_norm;  // 1: the projection CTAs normalize and quantize x themselves (no K0)
     unsigned *status;
 };
 struct OprojArgs {
@@ -51,13 +52,16 @@ struct OprojArgs {
     const float *residual;
     const uint8_t *wo;
     const float *bo;
-    const uint8_t *aq8;  // [H*hd/32] Q8_0 blocks of the attention output
+    const uint8_t *aq8;    // [H*hd/32] Q8_0 blocks of the attention output
+    const uint8_t *apack;  // the same row packed (xpack_bytes), or null: unpack aq8
     const int32_t *d_pos;
     int D, QD, rows_per_cta, C;
     unsigned *status;
 };
 int launch_norm_q8(const QkvArgs &a, cudaStream_t s, bool pdl);
 int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl);
+// Whether launch_qkv's CTAs can normalize and quantize x themselves.
+bool qkv_fused_norm_ok(const QkvArgs &a);
 int launch_oproj(const OprojArgs &a, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);
 
@@ -76,6 +80,7 @@ struct AttnArgs {
     float *part;              // scratch: partial results
     float *out;               // [B][H*hd] fp32 attention output
     uint8_t *out_q8;          // [B][H*hd/32] Q8_0 blocks, or null
+    uint8_t *out_pack;        // [B] packed rows of those blocks (xpack_bytes each), or null
     const void *l2_prefetch;  // optional: bytes the next kernel reads, pulled into L2
     size_t l2_prefetch_bytes;
     unsigned *status;
