@@ -8,11 +8,11 @@
 //                   H/KV query heads that read it ("GQA-packed": each cache
 //                   row is read once per KV head).  A producer warp streams
 //                   8-row K and V tiles into a shared-memory ring through
-//                   the bulk-copy engine, keeping at_lookahead() tiles in
-//                   flight (refilled as tiles arrive, so they arrive one
-//                   after another instead of all at the end); six consumer
-//                   warps take tiles round-robin, each with its own online
-//                   softmax, and merge their states at the end.
+//                   the bulk-copy engine in stages of up to ~16 KB per
+//                   operand (at_la stages in flight); six
+//                   consumer warps take 8-row tiles round-robin, each with
+//                   its own online softmax, and merge their states at the
+//                   end.
 //   k_attn_combine  grid (H, hd/32, B).  Log-sum-exp merge of the S partial
 //                   records of one query head over one 32-wide slice of its
 //                   dims (= one Q8_0 block): the fp32 output and the block.
@@ -32,27 +32,49 @@ constexpr int AT_CONSUMERS = 6;                      // consumer warps per CTA
 constexpr int AT_THREADS = 32 * (AT_CONSUMERS + 1);  // + one producer warp
 constexpr int GMAX = 8;                              // query heads per KV head
 
-// Stage count: as many 8-row K+V stages as fit in 192 KB (at most 18),
-// rounded down to a multiple of AT_CONSUMERS.  Tile t lives in stage
-// t % NST and is consumed by warp t % AT_CONSUMERS; with NST a multiple of
-// AT_CONSUMERS, the warp that waits for tile t on its stage's full barrier
-// is the warp that consumed tile t - NST there, so the barrier is never two
-// phases behind and the parity wait cannot pass on a stale phase.
-__host__ __device__ constexpr int at_stage_bytes(int hd) { return 2 * AT_TILE * hd * 4; }
-__host__ __device__ constexpr int at_stages(int hd) {
-    return ((192 * 1024) / at_stage_bytes(hd) > 18 ? 18 : (192 * 1024) / at_stage_bytes(hd)) / AT_CONSUMERS *
-           AT_CONSUMERS;
+// The ring (192 KB) holds stages of RS rows of K and of V.  Long splits use
+// the largest power-of-two RS with at most 16 KB per operand (one bulk copy
+// of 16 KB for head_dim 32, 64, 128 and 256, 12 KB for 96).
+// An SM's copy engine takes one bulk copy per few hundred cycles whatever its
+// size, so 4 KB copies capped the stream near 3 TB/s while 16 KB copies
+// reach the HBM peak.  Short splits (fewer than 8 such stages) keep 8-row
+// stages, whose first tile arrives sooner.  Consumers always take 8-row
+// tiles: stage k holds tiles TPS*k .. TPS*k + TPS - 1.  The slot count NSS
+// makes TPS * NSS a multiple of AT_CONSUMERS: tile t goes to warp
+// t % AT_CONSUMERS, so the warp that waits for a slot's phase p also consumed
+// the slot's phase p - 1 and the parity wait can never pass on a stale phase.
+constexpr int AT_RING_BYTES = 192 * 1024;
+constexpr int AT_MAX_SLOTS = 48;
+// Large-stage height: the largest power-of-two multiple of 8 rows with at
+// most 16 KB per operand (tiles per stage a power of two: shifts, not
+// divisions, in the consumer loop).
+__host__ __device__ constexpr int at_rs_big(int hd) {
+    return hd * 4 * 128 <= 16384 ? 128 : hd * 4 * 64 <= 16384 ? 64 : hd * 4 * 32 <= 16384 ? 32 : hd * 4 * 16 <= 16384 ? 16 : 8;
 }
-// Tiles in flight per CTA: about 80 KB, so that the whole GPU keeps ~12 MB
-// of requests outstanding (enough to saturate HBM) while tiles still arrive
-// one after another instead of all at once.
-__host__ __device__ constexpr int at_lookahead(int hd) {
-    return (80 * 1024) / at_stage_bytes(hd) < 4 ? 4
-           : (80 * 1024) / at_stage_bytes(hd) > at_stages(hd) - 2 ? at_stages(hd) - 2
-                                                                   : (80 * 1024) / at_stage_bytes(hd);
+// Ring geometry of the two stage heights (compile-time constants in each
+// kernel instantiation: the consumer loop stays as lean as with fixed tiles).
+__host__ __device__ constexpr int at_rs(int hd, bool big) { return big ? at_rs_big(hd) : AT_TILE; }
+__host__ __device__ constexpr int at_ss_bytes(int hd, bool big) { return 2 * at_rs(hd, big) * hd * 4; }
+__host__ __device__ constexpr int at_nss_from(int hd, bool big, int n) {
+    return n <= 1 ? 1 : ((at_rs(hd, big) / AT_TILE * n) % AT_CONSUMERS == 0 ? n : at_nss_from(hd, big, n - 1));
 }
-static_assert(at_stages(32) % AT_CONSUMERS == 0 && at_stages(256) >= AT_CONSUMERS, "stage ring");
-static_assert(at_lookahead(256) < at_stages(256) && at_lookahead(32) < at_stages(32), "look-ahead exceeds the ring");
+__host__ __device__ constexpr int at_nss(int hd, bool big) {
+    return at_nss_from(hd, big, AT_RING_BYTES / at_ss_bytes(hd, big) > AT_MAX_SLOTS ? AT_MAX_SLOTS
+                                                                                    : AT_RING_BYTES / at_ss_bytes(hd, big));
+}
+// stages in flight: ~96 KB of large stages, ~80 KB of 8-row stages
+__host__ __device__ constexpr int at_la(int hd, bool big) {
+    return ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big) < 1 ? 1
+           : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big) > at_nss(hd, big) - 1
+               ? at_nss(hd, big) - 1
+               : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big);
+}
+// Large stages for splits of at least 8 of them.
+__host__ __device__ inline bool at_big(int hd, int chunk_rows) { return chunk_rows >= 8 * at_rs_big(hd); }
+static_assert(at_nss(32, true) >= 2 && at_nss(96, true) >= 2 && at_nss(128, true) >= 2 && at_nss(256, true) >= 2 &&
+                  at_nss(32, false) >= 2 && at_nss(256, false) >= 2,
+              "stage ring");
+
 // P row stride (floats): G heads, each duplicated into a pair, padded so
 // rows stay 16-byte aligned.
 __host__ __device__ constexpr int at_prow(int G) { return 2 * ((G + 1) & ~1); }
@@ -65,13 +87,13 @@ __host__ __device__ inline AttnSmem attn_smem(int hd) {
     AttnSmem L;
     size_t o = 0;
     L.off_full = o;
-    o += 18 * 8;
+    o += AT_MAX_SLOTS * 8;
     L.off_empty = o;
-    o += 18 * 8;
+    o += AT_MAX_SLOTS * 8;
     L.off_qbar = o;
     o += 16;
     L.off_stage = o;
-    o += static_cast<size_t>(at_stages(hd)) * at_stage_bytes(hd);
+    o += AT_RING_BYTES;
     L.off_q = o;
     o += static_cast<size_t>(GMAX) * hd * 4;
     L.off_p = o;
@@ -138,12 +160,10 @@ __device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][R], int slice
 // j's softmax state.
 // PV: lane = dims; each row adds p_j * v to GT accumulators, two dims per
 // packed FMA.
-template <int DPL, int GT>
+template <int DPL, int GT, bool BIG>
 __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) {
     constexpr int HD = 32 * DPL;
     constexpr int HD4 = HD / 4;
-    constexpr int NST = at_stages(HD);
-    constexpr int LA = at_lookahead(HD);
     constexpr int VEC = (DPL % 4 == 0) ? 4 : ((DPL % 2 == 0) ? 2 : 1);
     constexpr int NV = DPL / VEC;
     constexpr int PR = at_prow(GT);
@@ -202,44 +222,41 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     const float *kc = (a.k_caches ? a.k_caches[b] : a.k_cache) + static_cast<size_t>(g) * a.C * HD;
     const float *vc = (a.v_caches ? a.v_caches[b] : a.v_cache) + static_cast<size_t>(g) * a.C * HD;
     const int ntiles = (t1 - t0 + AT_TILE - 1) / AT_TILE;
+    constexpr int RS = at_rs(HD, BIG), TPS = RS / AT_TILE, NSS = at_nss(HD, BIG), LA = at_la(HD, BIG);
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        mbar_init(qbar, 1);
-        fence_mbar_init();
+    if (threadIdx.x < NSS) {  // one barrier pair per thread: a serial loop costs ~0.5 us
+        mbar_init(&full[threadIdx.x], 1);
+        mbar_init(&empty[threadIdx.x], TPS);  // every tile of the stage releases it
     }
+    if (threadIdx.x == AT_THREADS - 1) mbar_init(qbar, 1);
+    fence_mbar_init();
     __syncthreads();
     pdl_trigger();
 
     if (warp == 0) {
         // ---- producer.  Rows before T-1 are never written by the preceding
-        // grid, so they stream before waiting on it; the tile holding row
-        // T-1 (the row just stored) waits first.  Tile t is issued once tile
-        // t - LA has arrived and its stage is free.
+        // grid, so they stream before waiting on it; the super-stage holding
+        // row T-1 (the row just stored) waits first.  Super-stage k is issued
+        // once super-stage k - LA has arrived and its slot is free.
         if (lane == 0) {
-            bool ok = true;
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int st = t % NST;
-                if (t >= LA) {
-                    const int u = t - LA;
-                    ok = mbar_wait(&full[u % NST], (u / NST) & 1);
-                }
-                if (ok && t >= NST) ok = mbar_wait(&empty[st], ((t / NST) - 1) & 1);
+            const int nss = (t1 - t0 + RS - 1) / RS;
+            for (int k = 0; k < nss; ++k) {
+                const int sl = k % NSS;
+                bool ok = true;
+                if (k >= LA) ok = mbar_wait(&full[(k - LA) % NSS], ((k - LA) / NSS) & 1);
+                if (ok && k >= NSS) ok = mbar_wait(&empty[sl], ((k / NSS) - 1) & 1);
                 if (!ok) {
                     flag_error(a.status, FLAG_TIMEOUT);
                     break;
                 }
-                const int r = t0 + t * AT_TILE;
-                const int n = min(AT_TILE, t1 - r);
+                const int r = t0 + k * RS;
+                const int n = min(RS, t1 - r);
                 if (r + n >= T) pdl_wait();
-                float *dst = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
+                float *dst = stage + static_cast<size_t>(sl) * 2 * RS * HD;
                 const uint32_t bytes = static_cast<uint32_t>(n) * HD * 4;
-                mbar_arrive_expect_tx(&full[st], 2 * bytes);
-                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &full[st]);
-                bulk_g2s(dst + AT_TILE * HD, vc + static_cast<size_t>(r) * HD, bytes, &full[st]);
+                mbar_arrive_expect_tx(&full[sl], 2 * bytes);
+                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &full[sl]);
+                bulk_g2s(dst + RS * HD, vc + static_cast<size_t>(r) * HD, bytes, &full[sl]);
             }
         }
         return;
@@ -276,10 +293,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     }
 
     for (int t = cw; t < ntiles; t += AT_CONSUMERS) {
-        const int st = t % NST;
-        if (!mbar_wait(&full[st], (t / NST) & 1)) flag_error(a.status, FLAG_TIMEOUT);
-        const float *Kt = stage + static_cast<size_t>(st) * 2 * AT_TILE * HD;
-        const float *Vt = Kt + AT_TILE * HD;
+        const int k = t / TPS, st = k % NSS;
+        if (!mbar_wait(&full[st], (k / NSS) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+        const float *Kt = stage + static_cast<size_t>(st) * 2 * RS * HD + (t - k * TPS) * AT_TILE * HD;
+        const float *Vt = Kt + RS * HD;
         const int n = min(AT_TILE, t1 - (t0 + t * AT_TILE));
 
         // ---- scores, rows rl + 4k, in passes of k = {2p, 2p + 1}
@@ -560,7 +577,11 @@ template <int DPL, int GT>
 static int launch_attn_gt(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
     AttnArgs a = a0;
     const AttnSmem L = attn_smem(32 * DPL);
-    const void *fs = reinterpret_cast<const void *>(k_attn_split<DPL, GT>);
+    // stage height from the longest split (all splits of a launch share the plan)
+    const int T = a.d_pos ? a.C : a.kv_tokens;
+    const int chunk = a.chunk > 0 ? a.chunk : (T + a.splits - 1) / a.splits;
+    const void *fs = at_big(32 * DPL, chunk) ? reinterpret_cast<const void *>(k_attn_split<DPL, GT, true>)
+                                              : reinterpret_cast<const void *>(k_attn_split<DPL, GT, false>);
     ensure_smem(fs, L.total);
     void *args1[] = {&a};
     cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(AT_THREADS), L.total, s, pdl_first, args1);

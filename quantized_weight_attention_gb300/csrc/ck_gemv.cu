@@ -475,7 +475,58 @@ __device__ __forceinline__ QkvTask qkv_task(const QkvArgs &a, int t) {
     return T;
 }
 
-int qkv_tasks(const QkvArgs &a) { return (a.H + a.KV) * (a.hd >> 1) + ((a.KV * a.hd) >> 1); }
+__host__ __device__ int qkv_tasks(const QkvArgs &a) { return (a.H + a.KV) * (a.hd >> 1) + ((a.KV * a.hd) >> 1); }
+
+// Bulk copy of `bytes` (a multiple of 16) in pieces of at most 64 KB.  The
+// copy engine of an SM takes one bulk copy per few hundred cycles whatever its
+// size, so weight rows are staged in as few, large copies as possible.
+__device__ void bulk_g2s_run(uint8_t *dst, const uint8_t *src, uint32_t bytes, uint64_t *bar) {
+    for (uint32_t o = 0; o < bytes; o += 65536u) bulk_g2s(dst + o, src + o, bytes - o < 65536u ? bytes - o : 65536u, bar);
+}
+
+// Shared-memory rows of warp w's task: Q/K pairs go to an A block (row ra of
+// warp w at slot w) and a B block (row rb at slot nw + w), so that the rows
+// of consecutive RoPE pairs of one head are contiguous in both places; V
+// pairs (rows 2u, 2u + 1) sit side by side.
+__device__ __forceinline__ uint8_t *qkv_slot(uint8_t *wst, int kind, int w, int nw, int second, int rb5, int rb8) {
+    if (kind == 2) return wst + static_cast<size_t>(2 * w + second) * rb8;
+    return wst + static_cast<size_t>(second ? nw + w : w) * rb5;
+}
+
+// Thread 0: stage this CTA's Q/K/V rows, completing on `bar`.  When the
+// CTA's tasks are consecutive pairs of one head (or all V pairs), that is
+// two copies (one); otherwise two copies per task.
+__device__ void stage_qkv_rows(const QkvArgs &a, int nw, uint8_t *wst, uint64_t *bar, int rb5, int rb8) {
+    const int t0 = blockIdx.x * nw;
+    const int nt = min(nw, qkv_tasks(a) - t0);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    const QkvTask f = qkv_task(a, t0), l = qkv_task(a, t0 + nt - 1);
+    const uint8_t *Wf = f.kind == 0 ? a.wq : (f.kind == 1 ? a.wk : a.wv);
+    if (f.kind == 2 && l.kind == 2) {
+        const uint32_t bytes = static_cast<uint32_t>(2 * nt * rb8);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s_run(wst, Wf + static_cast<size_t>(f.ra) * rb8, bytes, bar);
+        return;
+    }
+    if (f.kind == l.kind && f.kind < 2 && f.head == l.head && l.i - f.i == nt - 1) {
+        const uint32_t bytes = static_cast<uint32_t>(nt * rb5);
+        mbar_arrive_expect_tx(bar, 2 * bytes);
+        bulk_g2s_run(wst, Wf + static_cast<size_t>(f.ra) * rb5, bytes, bar);
+        bulk_g2s_run(wst + static_cast<size_t>(nw) * rb5, Wf + static_cast<size_t>(f.rb) * rb5, bytes, bar);
+        return;
+    }
+    uint32_t total = 0;
+    for (int w = 0; w < nt; ++w) total += static_cast<uint32_t>(2 * (qkv_task(a, t0 + w).kind == 2 ? rb8 : rb5));
+    mbar_arrive_expect_tx(bar, total);
+    for (int w = 0; w < nt; ++w) {
+        const QkvTask T = qkv_task(a, t0 + w);
+        const uint8_t *W = T.kind == 0 ? a.wq : (T.kind == 1 ? a.wk : a.wv);
+        const int rb = T.kind == 2 ? rb8 : rb5;
+        bulk_g2s(qkv_slot(wst, T.kind, w, nw, 0, rb5, rb8), W + static_cast<size_t>(T.ra) * rb, rb, bar);
+        bulk_g2s(qkv_slot(wst, T.kind, w, nw, 1, rb5, rb8), W + static_cast<size_t>(T.rb) * rb, rb, bar);
+    }
+}
 
 // Sum over the segments [li, li + 16, ...) of one staged row, then over the
 // 16 lanes of each half-warp (lane 0: first row, lane 16: second row).
@@ -497,8 +548,8 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
     const int nb = a.D / QK, nseg = nb / 8;
     const int rb5 = nb * Q5B, rb8 = nb * Q8B;
     const ProjSmem L = proj_smem(1, nb, static_cast<size_t>(nw) * 2 * rb8);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp;
-    uint8_t *slot = smem + L.off_w + static_cast<size_t>(warp) * 2 * rb8;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);  // the CTA's weight rows
+    uint8_t *wst = smem + L.off_w;
     const XRow x = xrow_at(smem, L);
     const QkvTask T = qkv_task(a, blockIdx.x * nw + warp);
     const int pos = a.d_pos ? *a.d_pos : a.pos;
@@ -508,19 +559,7 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
         return;
     }
     const bool q8 = T.kind == 2;
-    const int rb = q8 ? rb8 : rb5;
-    if (lane == 0 && T.kind != 3) {  // the weights do not depend on earlier grids
-        const uint8_t *W = T.kind == 0 ? a.wq : (T.kind == 1 ? a.wk : a.wv);
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * rb));
-        if (q8) {
-            bulk_g2s(slot, W + static_cast<size_t>(T.ra) * rb, static_cast<uint32_t>(2 * rb), bar);
-        } else {
-            bulk_g2s(slot, W + static_cast<size_t>(T.ra) * rb, static_cast<uint32_t>(rb), bar);
-            bulk_g2s(slot + rb, W + static_cast<size_t>(T.rb) * rb, static_cast<uint32_t>(rb), bar);
-        }
-    }
+    if (threadIdx.x == 0) stage_qkv_rows(a, nw, wst, bar, rb5, rb8);  // the weights do not depend on earlier grids
     pdl_trigger();
     if (a.fused_norm) {
         float gv[NORM_XPW];  // gamma does not depend on the preceding grid
@@ -538,7 +577,7 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
     }
     if (T.kind == 3) return;
     if (!mbar_wait(bar, 0)) flag_error(a.status, FLAG_TIMEOUT);
-    const uint8_t *row = slot + (lane >> 4) * rb;
+    const uint8_t *row = qkv_slot(wst, T.kind, warp, nw, lane >> 4, rb5, rb8);
     const float acc = q8 ? warp_row_dot<true>(row, nseg, lane & 15, x) : warp_row_dot<false>(row, nseg, lane & 15, x);
     const float sb = __shfl_sync(0xffffffffu, acc, 16);
     if (lane != 0) return;
@@ -576,7 +615,7 @@ __global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
     const int nb = a.QD / QK, nseg = nb / 8;
     const int rb = nb * Q5B;
     const ProjSmem L = proj_smem(1, nb, static_cast<size_t>(nw) * 2 * rb);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem) + warp;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);  // the CTA's rows of Wo
     uint8_t *slot = smem + L.off_w + static_cast<size_t>(warp) * 2 * rb;
     const XRow x = xrow_at(smem, L);
     const int r0 = 2 * (blockIdx.x * nw + warp);
@@ -588,11 +627,13 @@ __global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
             return;
         }
     }
-    if (lane == 0 && valid) {
+    if (threadIdx.x == 0) {  // the CTA's rows are contiguous: one run of copies
+        const int rw0 = 2 * blockIdx.x * nw, rw1 = min(a.D, rw0 + 2 * nw);
+        const uint32_t bytes = static_cast<uint32_t>(rw1 - rw0) * rb;
         mbar_init(bar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(2 * rb));
-        bulk_g2s(slot, a.wo + static_cast<size_t>(r0) * rb, static_cast<uint32_t>(2 * rb), bar);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s_run(smem + L.off_w, a.wo + static_cast<size_t>(rw0) * rb, bytes, bar);
     }
     pdl_trigger();
     pdl_wait();  // the attention output is ready

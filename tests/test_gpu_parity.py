@@ -162,6 +162,10 @@ def test_kv_store_bitexact(dev):
 # --------------------------------------------------------------------------
 ATT = [(4, 2, 64, 17, 64), (14, 2, 64, 1025, 2048), (28, 4, 128, 8193, 8256), (8, 8, 32, 5, 8),
        (6, 2, 96, 100, 128), (8, 1, 256, 300, 512), (4, 4, 128, 33, 33), (2, 1, 64, 64, 64), (7, 1, 128, 4097, 5000)]
+# Splits long enough (at 8 KV heads) for the ~16 KB stages of every head_dim,
+# each ending in a partial stage; rows past kv_tokens are NaN.
+ATT_LONG = [(16, 8, 32, 20011, 20016), (56, 8, 64, 10003, 10010), (24, 8, 96, 6203, 6210), (64, 8, 128, 5011, 5016),
+            (8, 8, 256, 2517, 2520)]
 
 
 def _attn_case(Hh, KV, hd, Tn, C, seed):
@@ -185,7 +189,7 @@ def _gpu_attn(dev, qv, kc, vc, Hh, KV, hd, Tn, C):
     return H(out)
 
 
-@pytest.mark.parametrize("Hh,KV,hd,Tn,C", ATT)
+@pytest.mark.parametrize("Hh,KV,hd,Tn,C", ATT + ATT_LONG)
 def test_attention_parity(dev, Hh, KV, hd, Tn, C):
     qv, kc, vc = _attn_case(Hh, KV, hd, Tn, C, Hh * 1000 + Tn)
     got = _gpu_attn(dev, qv, kc, vc, Hh, KV, hd, Tn, C)
