@@ -202,6 +202,38 @@ int ck_device_status(int *status, void *stream);
 size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
                                       int cache_capacity);
 
+/* ---- a batch of sequences sharing the layer ----------------------------- */
+
+/* The decode step of the MAIN KERNEL for `batch` sequences that share the
+ * layer's weights, each with its own KV cache and position (the same result,
+ * sequence by sequence, as ck_decode_layer_devpos on that sequence; the
+ * weights are read once for the whole batch).
+ * out, x, residual: fp32 [batch, embed_dim] (device; out must not alias x or
+ * residual).  Weights, biases, gamma, rope tables and eps as for
+ * ck_decode_layer.  k_caches, v_caches: device arrays of `batch` pointers,
+ * each to a head-major fp32 cache [num_kv_heads, cache_capacity, head_dim]
+ * (16-byte aligned; the arrays and the caches are read on the device and not
+ * validated by the host).  d_pos: int32 [batch] (device): sequence s writes
+ * row d_pos[s] of its caches and attends rows 0..d_pos[s]; a sequence whose
+ * position is outside 0..cache_capacity-1 writes nothing and raises CK_ERANGE
+ * in the device status word.  Requirements: 1 <= batch <= 1024, embed_dim and
+ * num_heads*head_dim multiples of 256 up to 4096, and the attention
+ * requirements; otherwise CK_EINVAL.
+ * `scratch`: >= ck_decode_layer_batched_scratch_size(...) bytes of device
+ * memory (contents need no initialization; the size depends on the device). */
+size_t ck_decode_layer_batched_scratch_size(int batch, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                            int cache_capacity);
+int ck_decode_layer_batched(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                            const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
+                            const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch,
+                            int embed_dim, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
+                            float eps, void *scratch, size_t scratch_bytes, void *stream);
+/* Byte offset of a tap (CK_TAP_*) in a batched scratch buffer: the taps hold
+ * `batch` rows of the single-sequence layout, row s after row s-1. */
+size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim, int num_heads, int num_kv_heads,
+                                              int head_dim, int cache_capacity);
+
 /* ---- test access to the integer block dots ----------------------------- */
 
 /* The per-block int32 dots that the GEMVs above compute, with the same

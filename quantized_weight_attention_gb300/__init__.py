@@ -59,6 +59,9 @@ _SIGS = {
     "ck_decode_layer_devpos": (_I, [_P] * 17 + [_I] * 5 + [_F, _P, _SZ, _P]),
     "ck_device_status": (_I, [_P, _P]),
     "ck_decode_layer_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "ck_decode_layer_batched_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "ck_decode_layer_batched": (_I, [_P] * 17 + [_I] * 6 + [_F, _P, _SZ, _P]),
+    "ck_decode_layer_batched_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "ck_block_dots_q5_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
     "ck_block_dots_q8_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
 }
@@ -190,6 +193,30 @@ CK_TAP_Q, CK_TAP_XQ8, CK_TAP_ATTN, CK_TAP_AQ8 = 0, 1, 2, 3
 def ck_decode_layer_scratch_offset(tap: int, embed_dim: int, num_heads: int, num_kv_heads: int, head_dim: int,
                                    cache_capacity: int) -> int:
     return lib().ck_decode_layer_scratch_offset(tap, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity)
+
+
+def ck_decode_layer_batched_scratch_size(batch: int, embed_dim: int, num_heads: int, num_kv_heads: int,
+                                        head_dim: int, cache_capacity: int) -> int:
+    return lib().ck_decode_layer_batched_scratch_size(batch, embed_dim, num_heads, num_kv_heads, head_dim,
+                                                      cache_capacity)
+
+
+def ck_decode_layer_batched(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_caches, v_caches, rope_cos,
+                            rope_sin, d_pos, batch: int, embed_dim: int, num_heads: int, num_kv_heads: int,
+                            head_dim: int, cache_capacity: int, eps: float, scratch, scratch_bytes: int,
+                            stream=None) -> int:
+    """k_caches / v_caches: device arrays of `batch` cache pointers (e.g. int64 tensors of data_ptr()s)."""
+    return lib().ck_decode_layer_batched(
+        _ptr(out), _ptr(x), _ptr(residual), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _ptr(gamma), _ptr(bq), _ptr(bk),
+        _ptr(bv), _ptr(bo), _ptr(k_caches), _ptr(v_caches), _ptr(rope_cos), _ptr(rope_sin), _ptr(d_pos), batch,
+        embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps, _ptr(scratch), scratch_bytes,
+        _stream(stream))
+
+
+def ck_decode_layer_batched_scratch_offset(tap: int, batch: int, embed_dim: int, num_heads: int, num_kv_heads: int,
+                                           head_dim: int, cache_capacity: int) -> int:
+    return lib().ck_decode_layer_batched_scratch_offset(tap, batch, embed_dim, num_heads, num_kv_heads, head_dim,
+                                                        cache_capacity)
 
 
 def ck_block_dots_q5_0_q8_0(isum, W, x_q8, M: int, K: int, stream=None) -> int:

@@ -148,6 +148,41 @@ LayerScratch layer_scratch(int D, int H, int KV, int hd, int C) {
     return L;
 }
 
+struct BatchScratch {
+    size_t off_q, off_xq8, off_attn, off_aq8, off_xpack, off_apack, off_part, total;
+    int splits;
+};
+
+BatchScratch batch_scratch(int B, int D, int H, int KV, int hd, int C) {
+    BatchScratch L{};
+    L.splits = attn_splits_batched(B, KV, C);
+    const size_t nb = static_cast<size_t>(D / 32), nbo = static_cast<size_t>(H * hd / 32);
+    size_t o = 0;
+    L.off_q = o;
+    o = a256(o + static_cast<size_t>(B) * H * hd * 4);
+    L.off_xq8 = o;
+    o = a256(o + static_cast<size_t>(B) * nb * 34);
+    L.off_attn = o;
+    o = a256(o + static_cast<size_t>(B) * H * hd * 4);
+    L.off_aq8 = o;
+    o = a256(o + static_cast<size_t>(B) * nbo * 34);
+    L.off_xpack = o;
+    o = a256(o + static_cast<size_t>(B) * xpack_bytes(static_cast<int>(nb)));
+    L.off_apack = o;
+    o = a256(o + static_cast<size_t>(B) * xpack_bytes(static_cast<int>(nbo)));
+    L.off_part = o;
+    o = a256(o + attn_part_bytes(B, H, KV, hd, L.splits));
+    L.total = o;
+    return L;
+}
+
+int batch_shape_check(int B, int D, int H, int KV, int hd, int C) {
+    if (B < 1 || B > 1024 || D <= 0 || C <= 0) return CK_EINVAL;
+    int rc = attn_shape_ok(H, KV, hd);
+    if (rc) return rc;
+    return batched_shape_ok(D, H, hd) ? CK_OK : CK_EINVAL;
+}
+
 int layer_common(float *out, const float *x, const float *residual, const void *wq, const void *wk, const void *wv,
                  const void *wo, const float *gamma, const float *bq, const float *bk, const float *bv,
                  const float *bo, float *k_cache, float *v_cache, const float *rope_cos, const float *rope_sin,
@@ -362,6 +397,101 @@ int ck_decode_layer_devpos(float *out, const float *x, const float *residual, co
     return layer_common(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
                         rope_sin, 0, d_pos, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps,
                         scratch, scratch_bytes, stream);
+}
+
+size_t ck_decode_layer_batched_scratch_size(int batch, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                            int cache_capacity) {
+    if (batch_shape_check(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity)) return 0;
+    return batch_scratch(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity).total;
+}
+
+size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim, int num_heads, int num_kv_heads,
+                                              int head_dim, int cache_capacity) {
+    if (batch_shape_check(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))
+        return static_cast<size_t>(-1);
+    const BatchScratch L = batch_scratch(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
+    switch (tap) {
+        case CK_TAP_Q: return L.off_q;
+        case CK_TAP_XQ8: return L.off_xq8;
+        case CK_TAP_ATTN: return L.off_attn;
+        case CK_TAP_AQ8: return L.off_aq8;
+        default: return static_cast<size_t>(-1);
+    }
+}
+
+int ck_decode_layer_batched(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                            const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
+                            const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch,
+                            int embed_dim, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
+                            float eps, void *scratch, size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_caches, v_caches, rope_cos, rope_sin, d_pos},
+                        {bq, bk, bv, bo});
+    if (rc) return rc;
+    if ((rc = batch_shape_check(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))) return rc;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    const BatchScratch L = batch_scratch(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
+    if (scratch_bytes < L.total) return CK_ESCRATCH;
+    if (out == x || out == residual) return CK_EINVAL;
+    uint8_t *sc = static_cast<uint8_t *>(scratch);
+    cudaStream_t s = as_stream(stream);
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
+
+    BatchArgs ba{};
+    ba.B = batch;
+    ba.x = x;
+    ba.residual = residual;
+    ba.gamma = gamma;
+    ba.wq = static_cast<const uint8_t *>(wq);
+    ba.wk = static_cast<const uint8_t *>(wk);
+    ba.wv = static_cast<const uint8_t *>(wv);
+    ba.wo = static_cast<const uint8_t *>(wo);
+    ba.bq = bq;
+    ba.bk = bk;
+    ba.bv = bv;
+    ba.bo = bo;
+    ba.k_caches = k_caches;
+    ba.v_caches = v_caches;
+    ba.rope_cos = rope_cos;
+    ba.rope_sin = rope_sin;
+    ba.d_pos = d_pos;
+    ba.D = embed_dim;
+    ba.H = num_heads;
+    ba.KV = num_kv_heads;
+    ba.hd = head_dim;
+    ba.C = cache_capacity;
+    ba.eps = eps;
+    ba.out = out;
+    ba.q = reinterpret_cast<float *>(sc + L.off_q);
+    ba.xq8 = sc + L.off_xq8;
+    ba.xpack = sc + L.off_xpack;
+    ba.apack = sc + L.off_apack;
+    ba.status = st;
+    if (launch_norm_pack(ba, s, true)) return CK_ECUDA;
+    if (launch_rows_batched(ba, false, s, true)) return CK_ECUDA;
+
+    AttnArgs aa{};
+    aa.q = ba.q;
+    aa.k_caches = k_caches;
+    aa.v_caches = v_caches;
+    aa.d_pos = d_pos;
+    aa.H = num_heads;
+    aa.KV = num_kv_heads;
+    aa.hd = head_dim;
+    aa.C = cache_capacity;
+    aa.splits = L.splits;
+    aa.part = reinterpret_cast<float *>(sc + L.off_part);
+    aa.out = reinterpret_cast<float *>(sc + L.off_attn);
+    aa.out_q8 = sc + L.off_aq8;
+    aa.out_pack = ba.apack;
+    aa.l2_prefetch = wo;
+    aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
+    aa.status = st;
+    if (launch_attention(aa, batch, s, true, true)) return CK_ECUDA;
+    if (launch_rows_batched(ba, true, s, true)) return CK_ECUDA;
+    return CK_OK;
 }
 
 size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,

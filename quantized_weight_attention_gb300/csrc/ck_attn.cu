@@ -51,6 +51,19 @@ int attn_splits(int B, int KV, int max_tokens) {
     return S;
 }
 
+// Batches of many sequences: about 8 CTAs per SM so that the ragged lengths
+// balance across the grid; few sequences: one CTA per SM, as attn_splits.
+int attn_splits_batched(int B, int KV, int max_tokens) {
+    const int nsm = device_info().num_sms;
+    if (2 * B * KV <= nsm) return attn_splits(B, KV, max_tokens);
+    int S = (8 * nsm + B * KV - 1) / (B * KV);
+    const int tiles = (max_tokens + AT_TILE - 1) / AT_TILE;
+    if (S > tiles) S = tiles;
+    if (S < 1) S = 1;
+    if (S > 64) S = 64;
+    return S;
+}
+
 extern template int launch_attention_dpl<1>(const AttnArgs &, int, cudaStream_t, bool, bool);
 extern template int launch_attention_dpl<2>(const AttnArgs &, int, cudaStream_t, bool, bool);
 extern template int launch_attention_dpl<3>(const AttnArgs &, int, cudaStream_t, bool, bool);

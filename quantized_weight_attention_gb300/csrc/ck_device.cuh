@@ -228,6 +228,69 @@ __device__ __forceinline__ float seg_dot(const uint4 *seg, const XRow &x, int b0
     return acc;
 }
 
+// ---------------------------------------------------------------------------
+// Weight segments decoded ahead of the activation (batched projections): the
+// 8 blocks of one row segment as byte codes (Q5_0: q in 0..31 with the high
+// bit merged; Q8_0: the signed codes) plus the block scales, held in
+// registers and reused for every activation row.
+// ---------------------------------------------------------------------------
+struct SegCodes {
+    uint32_t c[8][8];
+    float d[8];
+};
+
+template <bool Q8>
+__device__ __forceinline__ void seg_decode(const uint8_t *src, SegCodes &R) {
+    using S = SegShape<Q8>;
+    const uint4 *seg = reinterpret_cast<const uint4 *>(src);
+    uint32_t w[S::WORDS + 1];
+#pragma unroll
+    for (int i = 0; i < S::CHUNKS; ++i) {
+        const uint4 v = __ldg(seg + i);
+        w[4 * i + 0] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    w[S::WORDS] = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int o = S::BLK * j;
+        R.d[j] = half_bits_to_float(at16(w, o));
+        if constexpr (Q8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) R.c[j][i] = at32(w, o + 2 + 4 * i);
+        } else {
+            const uint32_t qh = at32(w, o + 2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t qs = at32(w, o + 6 + 4 * i);
+                R.c[j][i] = (qs & 0x0F0F0F0Fu) | ((((qh >> (4 * i)) & 0xFu) * 0x02040810u) & 0x10101010u);
+                R.c[j][4 + i] =
+                    ((qs >> 4) & 0x0F0F0F0Fu) | ((((qh >> (16 + 4 * i)) & 0xFu) * 0x02040810u) & 0x10101010u);
+            }
+        }
+    }
+}
+
+// sum_j d_w d_x isum_j over the decoded segment's blocks b0..b0+7 (fp32, in
+// block order, as seg_dot); q5 subtracts the 16 * sum(x) offset of Q5_0.
+__device__ __forceinline__ float seg_dot_codes(const SegCodes &R, const XRow &x, int b0, bool q5) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int b = b0 + j;
+        int xw[8];
+        load_x_words(x, b, xw);
+        int s = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s = __dp4a(static_cast<int>(R.c[j][i]), xw[i], s);
+        if (q5) s -= 16 * x.sum[b];
+        acc = fmaf(static_cast<float>(s), R.d[j] * x.d[b], acc);
+    }
+    return acc;
+}
+
 // One block read straight from global memory at byte offset `ob` (even) of
 // a 16-byte aligned matrix, without touching bytes outside the block.
 template <bool Q8>
@@ -318,6 +381,110 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     s = __fadd_rn(a, b);
     const float bp = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm + Q8_0 of an activation row
+// ---------------------------------------------------------------------------
+// rstd = 1/sqrt(mean + eps) from every thread's (sum, compensation) pair of
+// x^2 terms: the pairs are combined with two-sums (warp, then CTA), so the
+// total equals the double-precision sum to ~2^-46 relative; rstd is then
+// formed in double and rounded once to fp32.  `red` holds 2*warps + 1
+// floats.  Every thread of the CTA gets rstd.
+__device__ inline float rstd_from_pairs(float s, float c, int D, float eps, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float t, err;
+        two_sum(s, s2, t, err);
+        s = t;
+        c = __fadd_rn(__fadd_rn(c, c2), err);
+    }
+    if (lane == 0) {
+        red[2 * warp] = s;
+        red[2 * warp + 1] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        s = lane < nw ? red[2 * lane] : 0.0f;
+        c = lane < nw ? red[2 * lane + 1] : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+            float t, err;
+            two_sum(s, s2, t, err);
+            s = t;
+            c = __fadd_rn(__fadd_rn(c, c2), err);
+        }
+        if (lane == 0) {
+            const double ss = static_cast<double>(s) + static_cast<double>(c);
+            red[2 * nw] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
+        }
+    }
+    __syncthreads();
+    return red[2 * nw];
+}
+
+// Accumulate v^2 into the unevaluated pair (s, c): two-sum of the rounded
+// square plus its exact FMA residual.
+__device__ __forceinline__ void sumsq_add(float v, float &s, float &c) {
+    const float p = __fmul_rn(v, v);
+    const float e = fmaf(v, v, -p);
+    float t, err;
+    two_sum(s, p, t, err);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(err, e));
+}
+
+// RMSNorm + quantize_row_q8_0 of the whole input row straight into this
+// CTA's shared-memory XRow (the projection prologue): warp w takes blocks
+// w, w + W, ... (at most NORM_XPW of them), every load of x is issued before
+// any is used, y = (x * rstd) * gamma in fp32, and the Q8_0 codes, scales and
+// code sums land in the XRow layout.  `gv` holds the warp's gamma values
+// (loaded before the wait on the preceding grid).  When `tap` is set the
+// Q8_0 blocks are also written there.
+constexpr int NORM_XPW = 8;
+__device__ inline void norm_quant_xrow(const float *x, const float (&gv)[NORM_XPW], int nb, int D, float eps, const XRow &xr,
+                                float *red, uint8_t *tap) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    float xv[NORM_XPW];
+    float s = 0.0f, c = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        const int b = warp + nw * j;
+        xv[j] = b < nb ? x[b * QK + lane] : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) sumsq_add(xv[j], s, c);
+    const float rstd = rstd_from_pairs(s, c, D, eps, red);
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        const int b = warp + nw * j;
+        if (b < nb) {  // warp-uniform
+            const float y = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
+            uint32_t dbits;
+            float dq;
+            const int q = q8_code(y, dbits, dq);
+            reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
+            const int sum = warp_isum(q);
+            if (lane == 0) {
+                xr.d[b] = dq;
+                xr.sum[b] = sum;
+            }
+            if (tap) {
+                uint8_t *o = tap + static_cast<size_t>(b) * Q8B;
+                o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+                if (lane == 0) {
+                    o[0] = static_cast<uint8_t>(dbits & 0xFF);
+                    o[1] = static_cast<uint8_t>(dbits >> 8);
+                }
+            }
+        }
+    }
+    __syncthreads();
 }
 
 }  // namespace ck

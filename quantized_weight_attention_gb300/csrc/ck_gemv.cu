@@ -102,59 +102,6 @@ __device__ void xrow_from_q8(const uint8_t *xq8, int nb, const XRow &x, uint32_t
     __syncthreads();  // the row is complete before any warp reads it
 }
 
-// rstd = 1/sqrt(mean + eps) from every thread's (sum, compensation) pair of
-// x^2 terms: the pairs are combined with two-sums (warp, then CTA), so the
-// total equals the double-precision sum to ~2^-46 relative; rstd is then
-// formed in double and rounded once to fp32.  `red` holds 2*warps + 1
-// floats.  Every thread of the CTA gets rstd.
-__device__ float rstd_from_pairs(float s, float c, int D, float eps, float *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-        float t, err;
-        two_sum(s, s2, t, err);
-        s = t;
-        c = __fadd_rn(__fadd_rn(c, c2), err);
-    }
-    if (lane == 0) {
-        red[2 * warp] = s;
-        red[2 * warp + 1] = c;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        s = lane < nw ? red[2 * lane] : 0.0f;
-        c = lane < nw ? red[2 * lane + 1] : 0.0f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-            const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-            float t, err;
-            two_sum(s, s2, t, err);
-            s = t;
-            c = __fadd_rn(__fadd_rn(c, c2), err);
-        }
-        if (lane == 0) {
-            const double ss = static_cast<double>(s) + static_cast<double>(c);
-            red[2 * nw] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
-        }
-    }
-    __syncthreads();
-    return red[2 * nw];
-}
-
-// Accumulate v^2 into the unevaluated pair (s, c): two-sum of the rounded
-// square plus its exact FMA residual.
-__device__ __forceinline__ void sumsq_add(float v, float &s, float &c) {
-    const float p = __fmul_rn(v, v);
-    const float e = fmaf(v, v, -p);
-    float t, err;
-    two_sum(s, p, t, err);
-    s = t;
-    c = __fadd_rn(c, __fadd_rn(err, e));
-}
-
 // rstd of RMSNorm (rmsnorm_forward, T = 1) over x[0..D), for every thread
 // of the CTA.  All loads of x are issued before any is used.
 __device__ float block_rstd(const float *x, int D, float eps, float *red) {
@@ -171,54 +118,6 @@ __device__ float block_rstd(const float *x, int D, float eps, float *red) {
         for (int k = 0; k < PE; ++k) sumsq_add(v[k], s, c);
     }
     return rstd_from_pairs(s, c, D, eps, red);
-}
-
-// RMSNorm + quantize_row_q8_0 of the whole input row straight into this
-// CTA's shared-memory XRow (the projection prologue): warp w takes blocks
-// w, w + W, ... (at most NORM_XPW of them), every load of x is issued before
-// any is used, y = (x * rstd) * gamma in fp32, and the Q8_0 codes, scales and
-// code sums land in the XRow layout.  `gv` holds the warp's gamma values
-// (loaded before the wait on the preceding grid).  When `tap` is set the
-// Q8_0 blocks are also written there.
-constexpr int NORM_XPW = 8;
-__device__ void norm_quant_xrow(const float *x, const float (&gv)[NORM_XPW], int nb, int D, float eps, const XRow &xr,
-                                float *red, uint8_t *tap) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    float xv[NORM_XPW];
-    float s = 0.0f, c = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NORM_XPW; ++j) {
-        const int b = warp + nw * j;
-        xv[j] = b < nb ? x[b * QK + lane] : 0.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < NORM_XPW; ++j) sumsq_add(xv[j], s, c);
-    const float rstd = rstd_from_pairs(s, c, D, eps, red);
-#pragma unroll
-    for (int j = 0; j < NORM_XPW; ++j) {
-        const int b = warp + nw * j;
-        if (b < nb) {  // warp-uniform
-            const float y = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
-            uint32_t dbits;
-            float dq;
-            const int q = q8_code(y, dbits, dq);
-            reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
-            const int sum = warp_isum(q);
-            if (lane == 0) {
-                xr.d[b] = dq;
-                xr.sum[b] = sum;
-            }
-            if (tap) {
-                uint8_t *o = tap + static_cast<size_t>(b) * Q8B;
-                o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-                if (lane == 0) {
-                    o[0] = static_cast<uint8_t>(dbits & 0xFF);
-                    o[1] = static_cast<uint8_t>(dbits >> 8);
-                }
-            }
-        }
-    }
-    __syncthreads();
 }
 
 // A packed activation row (the XRow image, written by its producer kernel)

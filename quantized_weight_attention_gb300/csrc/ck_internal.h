@@ -63,6 +63,28 @@ int launch_qkv(const QkvArgs &a, cudaStream_t s, bool pdl);
 // Whether launch_qkv's CTAs can normalize and quantize x themselves.
 bool qkv_fused_norm_ok(const QkvArgs &a);
 int launch_oproj(const OprojArgs &a, cudaStream_t s, bool pdl);
+
+// The batched step (ck_batched.cu).
+struct BatchArgs {
+    int B;
+    const float *x, *residual, *gamma;
+    const uint8_t *wq, *wk, *wv, *wo;
+    const float *bq, *bk, *bv, *bo;
+    float *const *k_caches, *const *v_caches;  // device arrays [B]
+    const float *rope_cos, *rope_sin;
+    const int32_t *d_pos;  // device [B]
+    int D, H, KV, hd, C;
+    float eps;
+    float *out;      // [B][D]
+    float *q;        // [B][H*hd]
+    uint8_t *xq8;    // [B][D/32] Q8_0 blocks of the normed inputs
+    uint8_t *xpack;  // [B] packed rows of the normed inputs
+    uint8_t *apack;  // [B] packed rows of the attention outputs
+    unsigned *status;
+};
+bool batched_shape_ok(int D, int H, int hd);
+int launch_norm_pack(const BatchArgs &a, cudaStream_t s, bool pdl);
+int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);
 
 // ---- attention (ck_attn.cu) ----
@@ -87,6 +109,7 @@ struct AttnArgs {
 };
 size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
 int attn_splits(int B, int KV, int max_tokens);
+int attn_splits_batched(int B, int KV, int max_tokens);
 int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine);
 int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, int H, int KV, int hd, cudaStream_t s);
 int launch_kv_store(float *kc, float *vc, const float *k, const float *v, int pos, int KV, int C, int hd,

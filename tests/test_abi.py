@@ -131,3 +131,44 @@ def test_scratch_offsets_are_disjoint_and_inside():
         assert o1 + s1 <= o2
     assert all(o % 256 == 0 for o in offs)
     assert spans[-1][0] + spans[-1][1] <= total
+
+
+def _batched(**kw):
+    a = dict(out=A + 4096, x=A, res=A, kcs=A, vcs=A, dpos=A, B=3, D=256, H=4, KV=2, hd=64, C=64, scratch=A,
+             nbytes=1 << 30)
+    a.update(kw)
+    return q.ck_decode_layer_batched(a["out"], a["x"], a["res"], A, A, A, A, A, None, None, None, None, a["kcs"],
+                                     a["vcs"], A, A, a["dpos"], a["B"], a["D"], a["H"], a["KV"], a["hd"], a["C"],
+                                     1e-6, a["scratch"], a["nbytes"], 0)
+
+
+def test_batched_validation():
+    """Every bad argument is refused on the host, before any launch."""
+    assert _batched(B=0) == q.CK_EINVAL
+    assert _batched(B=1025) == q.CK_EINVAL
+    assert _batched(D=224) == q.CK_EINVAL          # embed_dim not a multiple of 256
+    assert _batched(D=4352) == q.CK_EINVAL         # more than 128 blocks per row
+    assert _batched(H=2, hd=64) == q.CK_EINVAL     # num_heads*head_dim = 128
+    assert _batched(H=6, KV=4) == q.CK_EINVAL
+    assert _batched(hd=48) == q.CK_EINVAL
+    assert _batched(kcs=None) == q.CK_EINVAL
+    assert _batched(dpos=None) == q.CK_EINVAL
+    assert _batched(dpos=MIS) == q.CK_EALIGN
+    assert _batched(scratch=None) == q.CK_ESCRATCH
+    assert _batched(nbytes=100) == q.CK_ESCRATCH
+    assert _batched(scratch=MIS) == q.CK_EALIGN
+    assert _batched(out=A) == q.CK_EINVAL           # out aliases x
+    assert q.ck_decode_layer_batched_scratch_size(0, 256, 4, 2, 64, 64) == 0
+    assert q.ck_decode_layer_batched_scratch_offset(9, 3, 256, 4, 2, 64, 64) == (1 << 64) - 1
+
+
+def test_batched_scratch_offsets_are_disjoint_and_inside():
+    Bn, D, H, KV, hd, C = 64, 3584, 28, 4, 128, 16448
+    total = q.ck_decode_layer_batched_scratch_size(Bn, D, H, KV, hd, C)
+    offs = [q.ck_decode_layer_batched_scratch_offset(t, Bn, D, H, KV, hd, C) for t in range(4)]
+    sizes = [Bn * H * hd * 4, Bn * D // 32 * 34, Bn * H * hd * 4, Bn * H * hd // 32 * 34]
+    spans = sorted(zip(offs, sizes))
+    for (o1, s1), (o2, _) in zip(spans, spans[1:]):
+        assert o1 + s1 <= o2
+    assert all(o % 256 == 0 for o in offs)
+    assert spans[-1][0] + spans[-1][1] <= total
