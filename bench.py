@@ -44,7 +44,7 @@ def parse():
     p.add_argument("--steps", type=int, default=60000)
     p.add_argument("--warmup", type=int, default=600)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="7b8k", choices=["tiny", "small1k", "7b8k", "stack32k"])
+    p.add_argument("--config", default="7b8k", choices=["tiny", "small1k", "7b8k", "stack32k", "batched64"])
     p.add_argument("--layers", type=int, default=0, help="stack32k: layers in the stack (default: all 28)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -214,6 +214,8 @@ def run_ours(args, ws, rank, local, pg):
     w = synth.WORKLOADS[args.config]
     if args.config == "stack32k":
         return run_stack(args, ws, pg, torch, q, synth, dev)
+    if args.config == "batched64":
+        return run_batched(args, ws, pg, torch, q, synth, dev)
     src = Source(torch, w, dev)
     per_replica = w.weight_bytes() + 2 * w.KV * w.capacity * w.hd * 4 + 4 * w.D * 8
     R = max(3, -(-int(2.5 * L2_BYTES) // per_replica))
@@ -432,6 +434,142 @@ def run_stack(args, ws, pg, torch, q, synth, dev):
             "gpu_launches": launches_per_layer(w) * nlayers * K, "clocks": clocks}
 
 
+def run_batched(args, ws, pg, torch, q, synth, dev):
+    """64 sequences of the 7B-shaped layer with ragged caches (lengths uniform
+    in [512, 16384]): one ck_decode_layer_batched call per step."""
+    w = synth.WORKLOADS["batched64"]
+    B = w.batch
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    lens = synth.batched_lengths(w, rng)
+    gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
+    x0 = rng.standard_normal((B, w.D)).astype(np.float32)
+    cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    g = dict(gamma=T(gamma), wq=T(wq), wk=T(wk), wv=T(wv), wo=T(wo), bq=T(bq), bk=T(bk), bv=T(bv), bo=T(bo),
+             cos=T(cos), sin=T(sin))
+    gen = torch.Generator(device=dev)
+    kcs, vcs = [], []
+    for s in range(B):
+        gen.manual_seed(w.seed * 1000 + s)
+        kc = torch.zeros((w.KV, w.capacity, w.hd), dtype=torch.float32, device=dev)
+        vc = torch.zeros_like(kc)
+        kc[:, :lens[s]].normal_(generator=gen)
+        vc[:, :lens[s]].normal_(generator=gen)
+        kcs.append(kc)
+        vcs.append(vc)
+    kptr = torch.tensor([c.data_ptr() for c in kcs], dtype=torch.int64, device=dev)
+    vptr = torch.tensor([c.data_ptr() for c in vcs], dtype=torch.int64, device=dev)
+    d_pos = T(lens)
+    xd = T(x0)
+    out = torch.empty((B, w.D), dtype=torch.float32, device=dev)
+    nbytes = q.ck_decode_layer_batched_scratch_size(B, w.D, w.H, w.KV, w.hd, w.capacity)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(xin):
+        q.check(q.ck_decode_layer_batched(out, xin, xin, g["wq"], g["wk"], g["wv"], g["wo"], g["gamma"], g["bq"],
+                                          g["bk"], g["bv"], g["bo"], kptr, vptr, g["cos"], g["sin"], d_pos, B, w.D,
+                                          w.H, w.KV, w.hd, w.capacity, w.eps, scratch, nbytes, stream.cuda_stream))
+
+    with torch.cuda.stream(stream):
+        step(xd)
+    torch.cuda.synchronize()
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(xd)
+    K, W = min(args.steps, 2000), max(args.warmup, 3)
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # a graph replays on the current stream
+        ev0.record(stream)
+        for _ in range(K):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    kv_bytes = int(sum((int(n) + 1) * w.KV * w.hd * 4 * 2 for n in lens))
+    per_step = w.weight_bytes() + kv_bytes
+    peak, peak_kind = measured_peaks()
+    ach = per_step * ws * K / sec / 1e9
+
+    # e2e: the B input rows from pinned host memory, the B output rows back
+    Ke = min(K, 200)
+    xh = torch.from_numpy(x0).pin_memory()
+    oh = torch.empty((B, w.D), dtype=torch.float32).pin_memory()
+    xe = torch.empty((B, w.D), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            xe.copy_(xh, non_blocking=True)
+            step(xe)
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1))
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    line = {"metric": METRIC, "value": round(ws * B * K / sec, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+            "warmup": W, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int8 dot (dp4a) + fp32", "data": "synthetic",
+            "config": {"workload": f"batched64: {B} sequences of the D=3584 28/4-head layer sharing its weights, "
+                                   f"cache lengths uniform in [{w.kv_lo}, {w.kv_hi}] (sum {int(sum(lens))}), "
+                                   f"one ck_decode_layer_batched call per step",
+                       "l2": f"{per_step / 1e9:.2f} GB per step >> L2"},
+            "step_hbm_gbs": round(ach, 1), "step_bytes": per_step,
+            "roofline": {"kernel": "whole batched step", "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(ach / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": None},
+            "e2e": {"value": round(ws * B * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": B * w.D * 4, "d2h_bytes_per_step": B * w.D * 4, "steps": Ke,
+                    "how": "per step: pinned x [B, D] -> device, ck_decode_layer_batched, out -> pinned host"},
+            "gpu_launches": 5 * K, "clocks": clocks}
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        line["cpu_baseline"] = cpu_baseline_batched(w, lens, gamma, wq, wk, wv, wo, bq, bk, bv, bo, x0, cos, sin,
+                                                    args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_batched(w, lens, gamma, wq, wk, wv, wo, bq, bk, bv, bo, x0, cos, sin, budget_s):
+    """The oracle's decode step run sequence after sequence (each on its own
+    cache) until budget_s: tokens/s over the sequences done (cache drawing is
+    not timed)."""
+    import oracle
+    oracle.lib()
+    rng = np.random.Generator(np.random.PCG64(w.seed + 100))
+    done, el = 0, 0.0
+    for s in range(w.batch):
+        kc = np.zeros((w.KV, w.capacity, w.hd), np.float32)
+        vc = np.zeros((w.KV, w.capacity, w.hd), np.float32)
+        n = int(lens[s])
+        kc[:, :n] = rng.standard_normal((w.KV, n, w.hd), dtype=np.float32)
+        vc[:, :n] = rng.standard_normal((w.KV, n, w.hd), dtype=np.float32)
+        t0 = time.perf_counter()
+        oracle.decode_layer(x0[s], x0[s], wq, wk, wv, wo, gamma, bq, bk, bv, bo, kc, vc, cos, sin, n, w.D, w.H, w.KV,
+                            w.hd, w.capacity, w.eps)
+        el += time.perf_counter() - t0
+        done += 1
+        if el >= budget_s:
+            break
+    return {"value": round(done / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of the {w.batch} sequences' decode steps (cache lengths "
+                      f"{', '.join(str(int(v)) for v in lens[:done])}) by the single-threaded C oracle, "
+                      f"{el:.1f} s, cpu: {cpu_model()}"}
+
+
 # --------------------------------------------------------------------------
 # the oracle on the host cores
 # --------------------------------------------------------------------------
@@ -474,6 +612,20 @@ def cpu_baseline(w, budget_s):
 def run_reference(args, ws):
     from quantized_weight_attention_gb300 import synth
     w = synth.WORKLOADS[args.config]
+    if args.config == "batched64":  # the oracle sequence after sequence, within a few minutes
+        rng = np.random.Generator(np.random.PCG64(w.seed))
+        lens = synth.batched_lengths(w, rng)
+        gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
+        x0 = rng.standard_normal((w.batch, w.D)).astype(np.float32)
+        cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+        cb = cpu_baseline_batched(w, lens, gamma, wq, wk, wv, wo, bq, bk, bv, bo, x0, cos, sin, 120.0)
+        return {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": ws,
+                "steps": 1, "warmup": 0, "ms_per_step": round(1e3 * w.batch / cb["value"], 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64 accumulation (C oracle)", "data": "synthetic",
+                "config": {"workload": f"{w.name} (same as the GPU arm)"},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
     # each step is one full oracle decode step; the number timed is capped so
     # that warm-up + timed steps end within a few minutes
     budget = 150.0

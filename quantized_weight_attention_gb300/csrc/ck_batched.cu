@@ -11,8 +11,9 @@
 //                  rows, or two Wo rows); lane l < 16 decodes segment l of the
 //                  first row, lane 16 + l segment l of the second, once, before
 //                  waiting on the preceding grid; then for every sequence the
-//                  lanes dot their segment with its activation row (L1/L2)
-//                  and lane 0 runs the epilogue: bias, RoPE at the sequence's
+//                  lanes dot their segment with its activation row (staged
+//                  in shared memory 16 rows at a time) and lane 0 runs the
+//                  epilogue: bias, RoPE at the sequence's
 //                  position and the q / K-row / V-row stores (Q/K/V), or bias
 //                  plus residual (O).
 //   attention      the split kernel of ck_attn_kernels.cuh with per-sequence
@@ -23,15 +24,6 @@
 #include "ck_internal.h"
 
 namespace ck {
-
-__device__ __forceinline__ XRow xrow_global(const uint8_t *pack, int nb) {
-    XRow x;
-    x.q = reinterpret_cast<int4 *>(const_cast<uint8_t *>(pack));
-    x.d = reinterpret_cast<float *>(const_cast<uint8_t *>(pack) + static_cast<size_t>(xq_chunks(nb)) * 16);
-    x.sum = reinterpret_cast<int *>(const_cast<uint8_t *>(pack) + static_cast<size_t>(xq_chunks(nb)) * 16 +
-                                    static_cast<size_t>(nb) * 4);
-    return x;
-}
 
 // Sequence s = blockIdx.x: RMSNorm + Q8_0 of x[s] into shared memory, then
 // the packed image to xpack[s] (and the Q8_0 blocks to xq8[s]).
@@ -98,12 +90,21 @@ __device__ __forceinline__ RowTask row_task(const BatchArgs &a, bool oproj, int 
     return T;
 }
 
+// Activation rows pass through shared memory in groups of BG sequences (two
+// buffers, filled by bulk copies while the other is in use), so each CTA
+// reads the batch's packed rows from L2 once instead of once per warp.
+constexpr int BG = 16;
+
 template <bool OPROJ>
 __global__ void __launch_bounds__(512, 1) k_rows_batched(const BatchArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int li = lane & 15;
     const int nb = OPROJ ? a.H * a.hd / QK : a.D / QK;  // blocks per weight row
     const int nseg = nb / 8;
+    const uint32_t pstride = static_cast<uint32_t>(xpack_bytes(nb));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);  // one per buffer
+    uint8_t *buf0 = smem + 128;
     const RowTask T = row_task(a, OPROJ, blockIdx.x * nw + warp);
     const bool q8 = T.kind == 2;
     SegCodes R;
@@ -115,57 +116,89 @@ __global__ void __launch_bounds__(512, 1) k_rows_batched(const BatchArgs a) {
         else
             seg_decode<false>(W + (static_cast<size_t>(row) * nb + li * 8) * Q5B, R);
     }
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
     pdl_trigger();
     pdl_wait();  // the packed activation rows are ready
-    if (T.kind == 3) return;
-    const size_t pstride = xpack_bytes(nb);
     const uint8_t *pack = OPROJ ? a.apack : a.xpack;
+    const int ngroups = (a.B + BG - 1) / BG;
+    auto fill = [&](int g) {  // thread 0: group g into buffer g % 2
+        const int n = min(BG, a.B - g * BG);
+        const uint32_t bytes = static_cast<uint32_t>(n) * pstride;
+        uint8_t *dst = buf0 + static_cast<size_t>(g & 1) * BG * pstride;
+        const uint8_t *src = pack + static_cast<size_t>(g) * BG * pstride;
+        mbar_arrive_expect_tx(&bar[g & 1], bytes);
+        for (uint32_t o = 0; o < bytes; o += 65536u)
+            bulk_g2s(dst + o, src + o, bytes - o < 65536u ? bytes - o : 65536u, &bar[g & 1]);
+    };
+    if (threadIdx.x == 0) {
+        fill(0);
+        if (ngroups > 1) fill(1);
+    }
     const int QD = a.H * a.hd, half = a.hd >> 1;
-    for (int s = 0; s < a.B; ++s) {
-        const int pos = a.d_pos[s];
-        const XRow x = xrow_global(pack + static_cast<size_t>(s) * pstride, nb);
-        float acc = li < nseg ? seg_dot_codes(R, x, li * 8, !q8) : 0.0f;
-        acc += __shfl_xor_sync(0xffffffffu, acc, 8);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        const float sb = __shfl_sync(0xffffffffu, acc, 16);
-        if (lane != 0) continue;
-        if (pos < 0 || pos >= a.C) {  // this sequence's step writes nothing
-            flag_error(a.status, FLAG_RANGE);
-            continue;
+    for (int g = 0; g < ngroups; ++g) {
+        if (!mbar_wait(&bar[g & 1], (g >> 1) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+        const uint8_t *gb = buf0 + static_cast<size_t>(g & 1) * BG * pstride;
+        const int n = min(BG, a.B - g * BG);
+        for (int j = 0; j < n && T.kind != 3; ++j) {
+            const int s = g * BG + j;
+            const int pos = a.d_pos[s];
+            XRow x;
+            x.q = reinterpret_cast<int4 *>(const_cast<uint8_t *>(gb) + static_cast<size_t>(j) * pstride);
+            x.d = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(x.q) + static_cast<size_t>(xq_chunks(nb)) * 16);
+            x.sum = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(x.d) + static_cast<size_t>(nb) * 4);
+            float acc = li < nseg ? seg_dot_codes(R, x, li * 8, !q8) : 0.0f;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            const float sb = __shfl_sync(0xffffffffu, acc, 16);
+            if (lane != 0) continue;
+            if (pos < 0 || pos >= a.C) {  // this sequence's step writes nothing
+                flag_error(a.status, FLAG_RANGE);
+                continue;
+            }
+            if (OPROJ) {
+                float *o = a.out + static_cast<size_t>(s) * a.D;
+                const float *res = a.residual + static_cast<size_t>(s) * a.D;
+                o[T.ra] = (acc + (a.bo ? a.bo[T.ra] : 0.0f)) + res[T.ra];
+                o[T.rb] = (sb + (a.bo ? a.bo[T.rb] : 0.0f)) + res[T.rb];
+                continue;
+            }
+            if (q8) {
+                float *vc = a.v_caches[s];
+                const float va = acc + (a.bv ? a.bv[T.ra] : 0.0f);
+                const float vb = sb + (a.bv ? a.bv[T.rb] : 0.0f);
+                int h = T.ra / a.hd;
+                vc[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.ra - h * a.hd)] = va;
+                h = T.rb / a.hd;
+                vc[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.rb - h * a.hd)] = vb;
+                continue;
+            }
+            const float *bias = T.kind == 0 ? a.bq : a.bk;
+            const float A = acc + (bias ? bias[T.ra] : 0.0f);
+            const float B = sb + (bias ? bias[T.rb] : 0.0f);
+            const float c = a.rope_cos[static_cast<size_t>(pos) * half + T.i];
+            const float sn = a.rope_sin[static_cast<size_t>(pos) * half + T.i];
+            const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, sn));
+            const float B2 = __fadd_rn(__fmul_rn(A, sn), __fmul_rn(B, c));
+            if (T.kind == 0) {
+                a.q[static_cast<size_t>(s) * QD + T.ra] = A2;
+                a.q[static_cast<size_t>(s) * QD + T.rb] = B2;
+            } else {
+                float *kr = a.k_caches[s] + (static_cast<size_t>(T.head) * a.C + pos) * a.hd;
+                kr[T.i] = A2;
+                kr[T.i + half] = B2;
+            }
         }
-        if (OPROJ) {
-            float *o = a.out + static_cast<size_t>(s) * a.D;
-            const float *res = a.residual + static_cast<size_t>(s) * a.D;
-            o[T.ra] = (acc + (a.bo ? a.bo[T.ra] : 0.0f)) + res[T.ra];
-            o[T.rb] = (sb + (a.bo ? a.bo[T.rb] : 0.0f)) + res[T.rb];
-            continue;
-        }
-        if (q8) {
-            float *vc = a.v_caches[s];
-            const float va = acc + (a.bv ? a.bv[T.ra] : 0.0f);
-            const float vb = sb + (a.bv ? a.bv[T.rb] : 0.0f);
-            int h = T.ra / a.hd;
-            vc[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.ra - h * a.hd)] = va;
-            h = T.rb / a.hd;
-            vc[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.rb - h * a.hd)] = vb;
-            continue;
-        }
-        const float *bias = T.kind == 0 ? a.bq : a.bk;
-        const float A = acc + (bias ? bias[T.ra] : 0.0f);
-        const float B = sb + (bias ? bias[T.rb] : 0.0f);
-        const float c = a.rope_cos[static_cast<size_t>(pos) * half + T.i];
-        const float sn = a.rope_sin[static_cast<size_t>(pos) * half + T.i];
-        const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, sn));
-        const float B2 = __fadd_rn(__fmul_rn(A, sn), __fmul_rn(B, c));
-        if (T.kind == 0) {
-            a.q[static_cast<size_t>(s) * QD + T.ra] = A2;
-            a.q[static_cast<size_t>(s) * QD + T.rb] = B2;
-        } else {
-            float *kr = a.k_caches[s] + (static_cast<size_t>(T.head) * a.C + pos) * a.hd;
-            kr[T.i] = A2;
-            kr[T.i + half] = B2;
+        __syncthreads();  // every warp is done with this buffer
+        if (threadIdx.x == 0 && g + 2 < ngroups) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // reads before the copy's writes
+            fill(g + 2);
         }
     }
 }
@@ -192,7 +225,11 @@ int launch_rows_batched(const BatchArgs &a0, bool oproj, cudaStream_t s, bool pd
     void *args[] = {&a};
     const void *fn = oproj ? reinterpret_cast<const void *>(k_rows_batched<true>)
                            : reinterpret_cast<const void *>(k_rows_batched<false>);
-    return launch(fn, dim3((tasks + warps - 1) / warps), dim3(32 * warps), 0, s, pdl, args) == cudaSuccess ? 0 : -5;
+    const int nb = oproj ? a.H * a.hd / QK : a.D / QK;
+    const size_t smem = 128 + 2 * static_cast<size_t>(BG) * xpack_bytes(nb);
+    ensure_smem(fn, smem);
+    return launch(fn, dim3((tasks + warps - 1) / warps), dim3(32 * warps), smem, s, pdl, args) == cudaSuccess ? 0
+                                                                                                             : -5;
 }
 
 }  // namespace ck
