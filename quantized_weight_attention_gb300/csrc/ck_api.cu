@@ -468,9 +468,12 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
     ba.xq8 = sc + L.off_xq8;
     ba.xpack = sc + L.off_xpack;
     ba.apack = sc + L.off_apack;
+    ba.aq8 = sc + L.off_aq8;
     ba.status = st;
+    // projections on the tensor cores where the shapes allow, else dp4a
+    const bool tc = batched_tc_ok(embed_dim, num_heads, num_kv_heads, head_dim);
     if (launch_norm_pack(ba, s, true)) return CK_ECUDA;
-    if (launch_rows_batched(ba, false, s, true)) return CK_ECUDA;
+    if ((tc ? launch_rows_tc(ba, false, s, true) : launch_rows_batched(ba, false, s, true))) return CK_ECUDA;
 
     AttnArgs aa{};
     aa.q = ba.q;
@@ -490,7 +493,7 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
     aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
     aa.status = st;
     if (launch_attention(aa, batch, s, true, true)) return CK_ECUDA;
-    if (launch_rows_batched(ba, true, s, true)) return CK_ECUDA;
+    if ((tc ? launch_rows_tc(ba, true, s, true) : launch_rows_batched(ba, true, s, true))) return CK_ECUDA;
     return CK_OK;
 }
 

@@ -80,9 +80,13 @@ struct BatchArgs {
     uint8_t *xq8;    // [B][D/32] Q8_0 blocks of the normed inputs
     uint8_t *xpack;  // [B] packed rows of the normed inputs
     uint8_t *apack;  // [B] packed rows of the attention outputs
+    uint8_t *aq8;    // [B][H*hd/32] Q8_0 blocks of the attention outputs
     unsigned *status;
 };
 bool batched_shape_ok(int D, int H, int hd);
+// Tensor-core projections (ck_batched_tc.cu): shapes they take, and launch.
+bool batched_tc_ok(int D, int H, int KV, int hd);
+int launch_rows_tc(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 int launch_norm_pack(const BatchArgs &a, cudaStream_t s, bool pdl);
 int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);

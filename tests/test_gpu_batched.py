@@ -190,7 +190,8 @@ def test_batched_matches_single_sequence_calls(dev):
                                     g["bq"], g["bk"], g["bv"], g["bo"], kc, vc, g["cos"], g["sin"], dpos, w.D, w.H,
                                     w.KV, w.hd, w.capacity, w.eps, scratch, nbytes))
         assert_close(out[s], H(o), f"seq {s}")
-        assert np.array_equal(H(b.kc[s])[:, b.pos[s]], H(kc)[:, b.pos[s]])
+        assert_close(H(b.kc[s])[:, b.pos[s]], H(kc)[:, b.pos[s]], f"seq {s}: stored k")
+        assert_close(H(b.vc[s])[:, b.pos[s]], H(vc)[:, b.pos[s]], f"seq {s}: stored v")
 
 
 def test_batched_out_of_range_position_writes_nothing(dev):
