@@ -20,6 +20,7 @@ sequence has no data-parallel split that needs a collective).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -46,6 +47,8 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="7b8k", choices=["tiny", "small1k", "7b8k", "stack32k", "batched64"])
     p.add_argument("--layers", type=int, default=0, help="stack32k: layers in the stack (default: all 28)")
+    p.add_argument("--kv-cap", type=int, default=0,
+                   help="batched64: cap every cache at this many rows (a small case for profilers; not the workload)")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -443,6 +446,11 @@ def run_batched(args, ws, pg, torch, q, synth, dev):
     lens = synth.batched_lengths(w, rng)
     gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
     x0 = rng.standard_normal((B, w.D)).astype(np.float32)
+    capped = ""
+    if args.kv_cap > 0:
+        w = dataclasses.replace(w, capacity=min(w.capacity, args.kv_cap))
+        lens = np.minimum(lens, w.capacity - 1).astype(np.int32)
+        capped = f" (caches capped at {w.capacity} rows: a profiling case)"
     cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     g = dict(gamma=T(gamma), wq=T(wq), wk=T(wk), wv=T(wv), wo=T(wo), bq=T(bq), bk=T(bk), bv=T(bv), bo=T(bo),
@@ -524,10 +532,11 @@ def run_batched(args, ws, pg, torch, q, synth, dev):
     assert rc == 0 and st == 0, (rc, st)
     line = {"metric": METRIC, "value": round(ws * B * K / sec, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
             "warmup": W, "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "int8 dot (dp4a) + fp32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "int8/int5 codes: exact integer block dots (tcgen05 f16, dp4a), fp32",
+            "data": "synthetic",
             "config": {"workload": f"batched64: {B} sequences of the D=3584 28/4-head layer sharing its weights, "
                                    f"cache lengths uniform in [{w.kv_lo}, {w.kv_hi}] (sum {int(sum(lens))}), "
-                                   f"one ck_decode_layer_batched call per step",
+                                   f"one ck_decode_layer_batched call per step{capped}",
                        "l2": f"{per_step / 1e9:.2f} GB per step >> L2"},
             "step_hbm_gbs": round(ach, 1), "step_bytes": per_step,
             "roofline": {"kernel": "whole batched step", "bound": "hbm", "achieved": round(ach, 1), "peak": peak,

@@ -35,6 +35,7 @@ constexpr int TC_KG = 4 * TC_BPS;      // 8-element K groups per stage
 constexpr int TC_THREADS = 256;
 constexpr int TC_TMEM_COLS = TC_BPS * TC_N;  // 128
 constexpr uint32_t TC_SBO = TC_KG * 128;     // bytes between 8-row groups
+constexpr int TC_DWS = TC_M + 4;             // floats per block of the weight scales (bank spread)
 
 struct TcSmem {
     size_t a[2], b[2], dw[2], dx[2], ep, bar, tmem, total;
@@ -51,8 +52,8 @@ __host__ __device__ inline TcSmem tc_smem() {
         o += static_cast<size_t>(TC_N) * TC_BPS * 32 * 2;  // 8 KB
     }
     for (int i = 0; i < 2; ++i) {
-        L.dw[i] = o;
-        o += static_cast<size_t>(TC_M) * TC_BPS * 4;
+        L.dw[i] = o;  // dw[j][row], rows padded to TC_DWS
+        o += static_cast<size_t>(TC_DWS) * TC_BPS * 4;
     }
     for (int i = 0; i < 2; ++i) {
         L.dx[i] = o;  // 16-byte aligned: read as float4
@@ -184,12 +185,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
     // loads are in flight while the previous stage is read back: load_w
     // fetches the raw pairs of thread `tid` (TC_WPT pairs of a 256-thread
     // sweep), decode_w writes them to the operand tile.
+    // Item `it` of a sweep is row (it & 7) + 8 (it >> 5), pair (it >> 3) & 3:
+    // the 8 threads of a quarter-warp write the 8 rows of one core matrix
+    // (distinct banks) and a warp reads 8 rows x 4 pairs (contiguous bytes).
     constexpr int TC_WPT = TC_M * (TC_BPS / 2) / TC_THREADS;  // 2
     auto load_w = [&](int k, uint32_t (&raw)[TC_WPT][TC_PAIR_WORDS]) {
 #pragma unroll
         for (int u = 0; u < TC_WPT; ++u) {
             const int it = tid + u * TC_THREADS;
-            const int r = it / (TC_BPS / 2), p = it - r * (TC_BPS / 2);
+            const int r = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
             const int blk = k * TC_BPS + 2 * p;
             load_pair(W + static_cast<size_t>(rbase + r) * rb + static_cast<size_t>(blk) * (wq8 ? Q8B : Q5B), wq8,
                       true, raw[u]);
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
 #pragma unroll
         for (int u = 0; u < TC_WPT; ++u) {
             const int it = tid + u * TC_THREADS;
-            const int r = it / (TC_BPS / 2), p = it - r * (TC_BPS / 2);
+            const int r = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
             uint32_t c0[8], c1[8];
             float d0, d1;
             if (wq8)
@@ -210,8 +214,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
                 decode_q5_pair(raw[u], c0, c1, d0, d1);
             put_block(tile, r, 2 * p, c0, wbias);
             put_block(tile, r, 2 * p + 1, c1, wbias);
-            dw[r * TC_BPS + 2 * p] = d0;
-            dw[r * TC_BPS + 2 * p + 1] = d1;
+            dw[(2 * p) * TC_DWS + r] = d0;
+            dw[(2 * p + 1) * TC_DWS + r] = d1;
         }
     };
     // activation half of stage k (after the wait on the preceding grid);
@@ -221,7 +225,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
         float *dx = reinterpret_cast<float *>(smem + buf(L.dx, k));
         const int it = tid;
         if (it < TC_N * (TC_BPS / 2)) {
-            const int sl = it / (TC_BPS / 2), p = it - sl * (TC_BPS / 2);
+            const int sl = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
             const int s = s0 + sl;
             uint32_t c0[8], c1[8];
             float d0 = 0.0f, d1 = 0.0f;
@@ -305,7 +309,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
         if (!mbar_wait(bar, k & 1)) flag_error(a.status, FLAG_TIMEOUT);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         {
-            const float *dw = reinterpret_cast<const float *>(smem + buf(L.dw, k)) + r * TC_BPS;
+            const float *dw = reinterpret_cast<const float *>(smem + buf(L.dw, k)) + r;
             const float4 *dx = reinterpret_cast<const float4 *>(smem + buf(L.dx, k));
 #pragma unroll
             for (int jj = 0; jj < TC_BPS / 2; ++jj) {
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
                     : "r"(taddr + (static_cast<uint32_t>((warp & 3) * 32) << 16) + j * TC_N)
                     : "memory");
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                const float dwv = dw[j];
+                const float dwv = dw[j * TC_DWS];
 #pragma unroll
                 for (int q4 = 0; q4 < TC_N / 4; ++q4) {
                     const float4 d4 = dx[j * (TC_N / 4) + q4];
