@@ -16,6 +16,7 @@
 //   k_attn_combine  grid (H, hd/32, B).  Log-sum-exp merge of the S partial
 //                   records of one query head over one 32-wide slice of its
 //                   dims (= one Q8_0 block): the fp32 output and the block.
+//   k_attn_combine_w  the same merge for S <= 8, one warp per output block.
 //
 // Scores are kept in log2 units: s2 = (q.k) * log2(e)/sqrt(hd), weights
 // exp2(s2 - m2), which equals exp(s - m) of the definition.
@@ -472,6 +473,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     }
 }
 
+// Output block `blk` of query head h of sequence b: the fp32 values, and,
+// when requested, the Q8_0 block and its copy in the packed row.
+template <int HD>
+__device__ __forceinline__ void combine_store(const AttnArgs &a, int b, int h, int blk, int lane, float o) {
+    a.out[(static_cast<size_t>(b) * a.H + h) * HD + blk * 32 + lane] = o;
+    if (a.out_q8) {
+        uint32_t dbits;
+        float dq;
+        const int q = q8_code(o, dbits, dq);
+        uint8_t *qb = a.out_q8 + ((static_cast<size_t>(b) * a.H + h) * (HD / 32) + blk) * Q8B;
+        qb[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+        if (lane == 0) {
+            qb[0] = static_cast<uint8_t>(dbits & 0xFF);
+            qb[1] = static_cast<uint8_t>(dbits >> 8);
+        }
+        if (a.out_pack) {  // the same block in the packed row the O-projection copies
+            const int nbo = a.H * (HD / 32), bq = h * (HD / 32) + blk;
+            uint8_t *pk = a.out_pack + static_cast<size_t>(b) * xpack_bytes(nbo);
+            pk[static_cast<size_t>(xq_chunk(bq, lane >> 4)) * 16 + (lane & 15)] =
+                static_cast<uint8_t>(static_cast<int8_t>(q));
+            const int sum = warp_isum(q);
+            if (lane == 0) {
+                reinterpret_cast<float *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16)[bq] = dq;
+                reinterpret_cast<int *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16 + nbo * 4)[bq] = sum;
+            }
+        }
+    }
+}
+
 // Merge of the S partial records of one query head, for one 32-wide slice of
 // its dims (= one Q8_0 block of the output).  Each warp loads its splits'
 // records in one round, merges them locally, then warp 0 merges the warps.
@@ -546,31 +576,62 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
                 L = fmaf(sc, lred[w], L);
             }
         }
-        const float o = __fdiv_rn(t, L);
-        a.out[(static_cast<size_t>(b) * a.H + h) * HD + blk * 32 + lane] = o;
-        if (a.out_q8) {
-            uint32_t dbits;
-            float dq;
-            const int q = q8_code(o, dbits, dq);
-            uint8_t *qb = a.out_q8 + ((static_cast<size_t>(b) * a.H + h) * (HD / 32) + blk) * Q8B;
-            qb[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
-            if (lane == 0) {
-                qb[0] = static_cast<uint8_t>(dbits & 0xFF);
-                qb[1] = static_cast<uint8_t>(dbits >> 8);
-            }
-            if (a.out_pack) {  // the same block in the packed row the O-projection copies
-                const int nbo = a.H * (HD / 32), bq = h * (HD / 32) + blk;
-                uint8_t *pk = a.out_pack + static_cast<size_t>(b) * xpack_bytes(nbo);
-                pk[static_cast<size_t>(xq_chunk(bq, lane >> 4)) * 16 + (lane & 15)] =
-                    static_cast<uint8_t>(static_cast<int8_t>(q));
-                const int sum = warp_isum(q);
-                if (lane == 0) {
-                    reinterpret_cast<float *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16)[bq] = dq;
-                    reinterpret_cast<int *>(pk + static_cast<size_t>(xq_chunks(nbo)) * 16 + nbo * 4)[bq] = sum;
-                }
-            }
+        combine_store<HD>(a, b, h, blk, lane, __fdiv_rn(t, L));
+    }
+}
+
+// Few splits (at most AT_COMB_WARP_MAX, the batched step's case): one warp
+// per 32-wide output block merges all of its splits itself, in split order,
+// with the arithmetic of the second merge level above.  A CTA is 8 warps =
+// 8 consecutive blocks; grid ceil(B * H * hd/32 / 8).
+constexpr int AT_COMB_WARP_MAX = 8;
+template <int DPL>
+__global__ void __launch_bounds__(256) k_attn_combine_w(const AttnArgs a, int B) {
+    constexpr int HD = 32 * DPL;
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int blk = item % DPL, bh = item / DPL;
+    const int h = bh % a.H, b = bh / a.H;
+    if (b >= B) {
+        pdl_wait();
+        return;
+    }
+    if (a.d_pos) {
+        const int pos = a.d_pos[b];
+        if (pos < 0 || pos >= a.C) {
+            pdl_wait();
+            return;
         }
     }
+    const int G = a.H / a.KV;
+    const int g = h / G, j = h - g * G;
+    const int S = a.splits;
+    pdl_trigger();
+    pdl_wait();
+    const size_t ps = part_stride(G, HD);
+    const float *base = a.part + (static_cast<size_t>(b) * a.KV + g) * S * ps;
+    float mv[AT_COMB_WARP_MAX], lv[AT_COMB_WARP_MAX], av[AT_COMB_WARP_MAX];
+#pragma unroll
+    for (int s = 0; s < AT_COMB_WARP_MAX; ++s) {
+        const bool ok = s < S;
+        const float *r = base + static_cast<size_t>(ok ? s : 0) * ps;
+        mv[s] = ok ? r[j] : -INFINITY;
+        lv[s] = ok ? r[G + j] : 0.0f;
+        av[s] = ok ? r[2 * G + j * HD + blk * 32 + lane] : 0.0f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < AT_COMB_WARP_MAX; ++s) M = fmaxf(M, mv[s]);
+    float t = 0.0f, L = 0.0f;
+#pragma unroll
+    for (int s = 0; s < AT_COMB_WARP_MAX; ++s) {
+        if (mv[s] != -INFINITY) {
+            const float sc = exp2f(mv[s] - M);
+            t = fmaf(sc, av[s], t);
+            L = fmaf(sc, lv[s], L);
+        }
+    }
+    combine_store<HD>(a, b, h, blk, lane, __fdiv_rn(t, L));
 }
 
 template <int DPL, int GT>
@@ -586,9 +647,16 @@ static int launch_attn_gt(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_fi
     void *args1[] = {&a};
     cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(AT_THREADS), L.total, s, pdl_first, args1);
     if (e != cudaSuccess) return -5;
-    void *args2[] = {&a};
-    e = launch(reinterpret_cast<const void *>(k_attn_combine<DPL>), dim3(a.H, DPL, B), dim3(256), 0, s, pdl_combine,
-               args2);
+    if (a.splits <= AT_COMB_WARP_MAX) {
+        void *args2[] = {&a, &B};
+        const int items = B * a.H * DPL;
+        e = launch(reinterpret_cast<const void *>(k_attn_combine_w<DPL>), dim3((items + 7) / 8), dim3(256), 0, s,
+                   pdl_combine, args2);
+    } else {
+        void *args2[] = {&a};
+        e = launch(reinterpret_cast<const void *>(k_attn_combine<DPL>), dim3(a.H, DPL, B), dim3(256), 0, s,
+                   pdl_combine, args2);
+    }
     return e == cudaSuccess ? 0 : -5;
 }
 
