@@ -149,8 +149,10 @@ LayerScratch layer_scratch(int D, int H, int KV, int hd, int C) {
 }
 
 struct BatchScratch {
-    size_t off_q, off_xq8, off_attn, off_aq8, off_xpack, off_apack, off_part, total;
+    size_t off_q, off_xq8, off_attn, off_aq8, off_xpack, off_apack, off_part, off_ximg, off_aimg, off_ppart,
+        off_tickets, total;
     int splits;
+    TpPlan tp;
 };
 
 BatchScratch batch_scratch(int B, int D, int H, int KV, int hd, int C) {
@@ -172,6 +174,16 @@ BatchScratch batch_scratch(int B, int D, int H, int KV, int hd, int C) {
     o = a256(o + static_cast<size_t>(B) * xpack_bytes(static_cast<int>(nbo)));
     L.off_part = o;
     o = a256(o + attn_part_bytes(B, H, KV, hd, L.splits));
+    // tensor-core projections: operand images, partial tiles, tile tickets
+    L.tp = tp_plan(B, D, H, KV, hd, false);
+    L.off_ximg = o;
+    o = a256(o + img_bytes(static_cast<int>(nb), B));
+    L.off_aimg = o;
+    o = a256(o + img_bytes(static_cast<int>(nbo), B));
+    L.off_ppart = o;
+    o = a256(o + L.tp.part_bytes);
+    L.off_tickets = o;
+    o = a256(o + static_cast<size_t>(L.tp.tickets) * 4);
     L.total = o;
     return L;
 }
@@ -472,6 +484,14 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
     ba.status = st;
     // projections on the tensor cores where the shapes allow, else dp4a
     const bool tc = batched_tc_ok(embed_dim, num_heads, num_kv_heads, head_dim);
+    if (tc) {
+        ba.ximg = sc + L.off_ximg;
+        ba.aimg = sc + L.off_aimg;
+        ba.proj_part = reinterpret_cast<float *>(sc + L.off_ppart);
+        ba.tickets = reinterpret_cast<int *>(sc + L.off_tickets);
+        ba.tickets_o = L.tp.tickets_o;
+        ba.n_tickets = L.tp.tickets;
+    }
     if (launch_norm_pack(ba, s, true)) return CK_ECUDA;
     if ((tc ? launch_rows_tc(ba, false, s, true) : launch_rows_batched(ba, false, s, true))) return CK_ECUDA;
 
@@ -489,6 +509,8 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
     aa.out = reinterpret_cast<float *>(sc + L.off_attn);
     aa.out_q8 = sc + L.off_aq8;
     aa.out_pack = ba.apack;
+    aa.out_img = ba.aimg;
+    aa.img_groups = img_groups(batch);
     aa.l2_prefetch = wo;
     aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
     aa.status = st;

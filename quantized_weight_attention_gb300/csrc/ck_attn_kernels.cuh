@@ -110,9 +110,6 @@ __host__ __device__ inline AttnSmem attn_smem(int hd) {
 // Partial results: for (b, g, s) a record of G m's, G l's, G*hd acc's.
 __host__ __device__ inline size_t part_stride(int G, int hd) { return static_cast<size_t>(G) * (hd + 2); }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sptr(bar)) : "memory");
-}
 __device__ __forceinline__ void consumers_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * AT_CONSUMERS) : "memory");
 }
@@ -487,6 +484,13 @@ __device__ __forceinline__ void combine_store(const AttnArgs &a, int b, int h, i
         if (lane == 0) {
             qb[0] = static_cast<uint8_t>(dbits & 0xFF);
             qb[1] = static_cast<uint8_t>(dbits >> 8);
+        }
+        if (a.out_img) {  // the block in the tensor-core operand image: one fp16 code per lane
+            const int bq = h * (HD / 32) + blk;
+            const __half hq = __int2half_rn(q);
+            *reinterpret_cast<__half *>(a.out_img + img_code_off(a.img_groups, b, bq, lane >> 3) + (lane & 7) * 2) =
+                hq;
+            if (lane == 0) *reinterpret_cast<float *>(a.out_img + img_d_off(a.img_groups, b, bq)) = dq;
         }
         if (a.out_pack) {  // the same block in the packed row the O-projection copies
             const int nbo = a.H * (HD / 32), bq = h * (HD / 32) + blk;

@@ -45,11 +45,23 @@ __global__ void __launch_bounds__(512) k_norm_pack(const BatchArgs a) {
     }
     pdl_trigger();
     pdl_wait();  // x may be the previous layer's output
+    if (s == 0 && a.tickets)  // the tensor-core projections' tile tickets of this step
+        for (int i = threadIdx.x; i < a.n_tickets; i += blockDim.x) a.tickets[i] = 0;
     norm_quant_xrow(a.x + static_cast<size_t>(s) * a.D, gv, nb, a.D, a.eps, xr, red,
                     a.xq8 + static_cast<size_t>(s) * nb * Q8B);
     const int n16 = static_cast<int>(xpack_bytes(nb) / 16);
     int4 *dst = reinterpret_cast<int4 *>(a.xpack + static_cast<size_t>(s) * xpack_bytes(nb));
     for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = xr.q[i];
+    if (a.ximg) {  // the row in the tensor-core operand image: 8 codes per item, then the scales
+        const int G = img_groups(a.B);
+        for (int i = threadIdx.x; i < nb * 4; i += blockDim.x) {
+            const int b = i >> 2, e = i & 3;
+            const uint32_t *w = reinterpret_cast<const uint32_t *>(&xr.q[xq_chunk(b, e >> 1)]) + (e & 1) * 2;
+            *reinterpret_cast<uint4 *>(a.ximg + img_code_off(G, s, b, e)) = q8_codes_to_half8(w[0], w[1]);
+        }
+        for (int b = threadIdx.x; b < nb; b += blockDim.x)
+            *reinterpret_cast<float *>(a.ximg + img_d_off(G, s, b)) = xr.d[b];
+    }
 }
 
 // Rows of warp task t.  Q/K/V: the tasks of the single-sequence projection

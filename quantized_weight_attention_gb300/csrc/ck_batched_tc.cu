@@ -7,75 +7,79 @@
 // fp32 accumulator, so one MMA pair per 32-element block yields the exact
 // int32 block dots; the per-block scales differ per row and per sequence, so
 // every block gets its own TMEM accumulator, read back and folded in with
-// fmaf(isum, d_w * d_x, acc) in block order (the formula of the dp4a GEMVs).
+// fmaf(isum, d_w * d_x, acc) (the formula of the dp4a GEMVs).
 //
-// CTA (256 threads): 128 weight rows (MMA M) x 16 sequences (MMA N).  K runs
-// in stages of 8 blocks (256 codes): warps 4-7 convert the next stage's
-// weights (Q5_0 or Q8_0 rows, read from global memory two blocks at a time)
-// and activations (the Q8_0 blocks of each sequence) into fp16 operand tiles
-// in shared memory (K-major, no swizzle, 8-row x 16-byte core matrices; the
-// leading byte offset is the stride between core matrices along K, the
-// stride byte offset the stride between 8-row groups), while thread 0 issues
-// the current stage's 16 MMAs into 8 TMEM slots of 16 columns and warps 0-3
-// read them back (TMEM lane = weight row).  Operand tiles are double-
-// buffered; the TMEM slots are reused every stage.
+// CTA = 128 weight rows (MMA M) x NT sequences (MMA N, up to 64: every
+// weight row is converted once per 64 sequences) x a range of the K stages
+// (4 blocks = 128 codes each).  A tile's K range is split over S CTAs so
+// that the grid fills the GPU; the last CTA of a tile to finish sums the S
+// partial tiles in split order (deterministic) and runs the epilogue.
+//
+// Warp roles, linked by mbarrier rings (full / empty) with no CTA-wide
+// barrier in the main loop:
+//   producers (8 warps)  one pair of a row's blocks per thread and stage:
+//                        load (a stage ahead, in registers), decode into the
+//                        fp16 A tile (K-major, no swizzle, 8-row x 16-byte
+//                        core matrices) and the weight scales; 3 slots.
+//   MMA warp (1)         TMEM allocation; bulk copies of the activation
+//                        operand (codes + scales, written once per step in
+//                        the MMA layout by the kernel that produced the
+//                        activations; 4 slots); per stage 8 MMAs into 4 TMEM
+//                        accumulators of NT columns (2 slots), one commit.
+//   read-back (8 warps)  warp w: TMEM lanes 32 (w % 4).. (its rows), half the
+//                        columns; acc += dot * (d_w * d_x), two lanes per
+//                        packed fp32 instruction (each rounded as the scalar
+//                        fmaf); then frees the stage's slots.
 //
 // The epilogue (bias, RoPE at each sequence's position, q / K / V stores, or
-// bias + residual) is the one of the dp4a kernel, from the accumulators
-// exchanged through shared memory.
+// bias + residual) is the one of the dp4a kernel.
 #include "ck_device.cuh"
 #include "ck_internal.h"
 
 namespace ck {
 
-constexpr int TC_M = 128;              // weight rows per CTA
-constexpr int TC_N = 16;               // sequences per CTA
-constexpr int TC_BPS = 8;              // blocks per stage
-constexpr int TC_KG = 4 * TC_BPS;      // 8-element K groups per stage
-constexpr int TC_THREADS = 256;
-constexpr int TC_TMEM_COLS = TC_BPS * TC_N;  // 128
-constexpr uint32_t TC_SBO = TC_KG * 128;     // bytes between 8-row groups
-constexpr int TC_DWS = TC_M + 4;             // floats per block of the weight scales (bank spread)
+constexpr int TP_M = 128;                 // weight rows per CTA
+constexpr int TP_BPS = IMG_BPS;           // blocks per stage
+constexpr int TP_KG = IMG_KG;             // 8-code groups per stage
+constexpr uint32_t TP_SBO = TP_KG * 128;  // bytes between 8-row groups (A tiles and activation stages)
+constexpr int TP_DWS = TP_M + 4;          // floats per block of the weight scales (bank spread)
+constexpr int TP_MAX_SPLITS = 8;
+static_assert(TP_SBO == IMG_RG_BYTES, "activation stages share the A tile's core-matrix layout");
+// warp roles
+constexpr int TW_CONS = 8;                     // read-back warps 0..7
+constexpr int TW_PROD = 8;                     // conversion warps 8..15
+constexpr int TW_MMA_WARP = TW_CONS + TW_PROD;  // warp 16: TMEM, bulk copies, MMAs
+constexpr int TW_THREADS = 32 * (TW_MMA_WARP + 1);
+// rings: A tiles + weight scales, activation stages, TMEM slots
+constexpr int TW_NA = 3, TW_NB = 4, TW_NTM = 2;
+constexpr size_t TP_A_BYTES = static_cast<size_t>(TP_M) * TP_BPS * 32 * 2;  // 32 KB
+constexpr size_t TP_DW_BYTES = static_cast<size_t>(TP_DWS) * TP_BPS * 4;
 
-struct TcSmem {
-    size_t a[2], b[2], dw[2], dx[2], ep, bar, tmem, total;
+struct TpSmem {
+    size_t a, b, dw, bar, tmem, ticket, total;
 };
-__host__ __device__ inline TcSmem tc_smem() {
-    TcSmem L;
+__host__ __device__ inline TpSmem tp_smem() {
+    TpSmem L;
     size_t o = 0;
-    for (int i = 0; i < 2; ++i) {
-        L.a[i] = o;
-        o += static_cast<size_t>(TC_M) * TC_BPS * 32 * 2;  // 64 KB
-    }
-    for (int i = 0; i < 2; ++i) {
-        L.b[i] = o;
-        o += static_cast<size_t>(TC_N) * TC_BPS * 32 * 2;  // 8 KB
-    }
-    for (int i = 0; i < 2; ++i) {
-        L.dw[i] = o;  // dw[j][row], rows padded to TC_DWS
-        o += static_cast<size_t>(TC_DWS) * TC_BPS * 4;
-    }
-    for (int i = 0; i < 2; ++i) {
-        L.dx[i] = o;  // 16-byte aligned: read as float4
-        o += static_cast<size_t>(TC_N) * TC_BPS * 4;
-    }
-    L.ep = o;  // accumulators for the epilogue [TC_M][TC_N + 1]
-    o += static_cast<size_t>(TC_M) * (TC_N + 1) * 4;
+    L.a = o;  // TW_NA A tiles (later the sums [TP_M][NT + 1])
+    o += TW_NA * TP_A_BYTES;
+    L.b = o;  // TW_NB activation stages (codes + scales)
+    o += static_cast<size_t>(TW_NB) * IMG_STAGE_BYTES;
+    L.dw = o;  // TW_NA x dw[j][row]
+    o += TW_NA * TP_DW_BYTES;
     L.bar = o;
-    o += 16;
+    o += static_cast<size_t>(2 * TW_NA + 2 * TW_NB + 2 * TW_NTM) * 8;
     L.tmem = o;
+    o += 16;
+    L.ticket = o;
     o += 16;
     L.total = (o + 127) / 128 * 128;
     return L;
 }
 
-// Offset of double buffer `k & 1` without indexing the layout dynamically
-// (which would place it in local memory).
-__device__ __forceinline__ size_t buf(const size_t (&b)[2], int k) { return (k & 1) ? b[1] : b[0]; }
-
-__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {
+__device__ __forceinline__ uint64_t tp_desc(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((128u >> 4) & 0x3FFFu) << 16) |
-           (static_cast<uint64_t>((TC_SBO >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+           (static_cast<uint64_t>((TP_SBO >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
 // Four byte codes -> four fp16 values in two words: bytes u (unsigned) map to
@@ -89,32 +93,29 @@ __device__ __forceinline__ void codes_to_half(uint32_t c, __half2 bias, uint32_t
     hi = *reinterpret_cast<const uint32_t *>(&hb);
 }
 
-// Write one 32-element block (8 words of byte codes, element order) of row r
-// at stage block j into the operand tile `tile` (core-matrix layout).
+// One 32-element block (8 words of byte codes, element order) of row r at
+// stage block j into the A tile (core-matrix layout).
 __device__ __forceinline__ void put_block(uint8_t *tile, int r, int j, const uint32_t (&c)[8], __half2 bias) {
 #pragma unroll
     for (int g = 0; g < 4; ++g) {  // 8 elements each
         uint4 v;
         codes_to_half(c[2 * g], bias, v.x, v.y);
         codes_to_half(c[2 * g + 1], bias, v.z, v.w);
-        *reinterpret_cast<uint4 *>(tile + ((r >> 3) * TC_KG + 4 * j + g) * 128 + (r & 7) * 16) = v;
+        *reinterpret_cast<uint4 *>(tile + ((r >> 3) * TP_KG + 4 * j + g) * 128 + (r & 7) * 16) = v;
     }
 }
 
 // Two consecutive blocks of a row (Q5_0: 44 bytes, Q8_0: 68 bytes; 4-byte
-// aligned) as raw words: every load of a stage is issued before any is used.
-constexpr int TC_PAIR_WORDS = 17;
-__device__ __forceinline__ void load_pair(const uint8_t *src, bool q8, bool ldg, uint32_t (&w)[TC_PAIR_WORDS]) {
+// aligned) as raw words.
+constexpr int TP_PAIR_WORDS = 17;
+__device__ __forceinline__ void load_pair(const uint8_t *src, bool q8, uint32_t (&w)[TP_PAIR_WORDS]) {
     const uint32_t *p = reinterpret_cast<const uint32_t *>(src);
 #pragma unroll
-    for (int i = 0; i < TC_PAIR_WORDS; ++i) {
-        if (i < 11 || q8) w[i] = ldg ? __ldg(p + i) : __ldcg(p + i);
-        else w[i] = 0;
-    }
+    for (int i = 0; i < TP_PAIR_WORDS; ++i) w[i] = (i < 11 || q8) ? __ldg(p + i) : 0u;
 }
 
 // Raw Q5_0 pair -> codes q in 0..31 per element and the two scales.
-__device__ __forceinline__ void decode_q5_pair(const uint32_t (&w)[TC_PAIR_WORDS], uint32_t (&c0)[8], uint32_t (&c1)[8],
+__device__ __forceinline__ void decode_q5_pair(const uint32_t (&w)[TP_PAIR_WORDS], uint32_t (&c0)[8], uint32_t (&c1)[8],
                                                float &d0, float &d1) {
     // block 0 at byte 0: d = w0 low half, qh = bytes 2..5, qs = bytes 6..21
     d0 = half_bits_to_float(w[0]);
@@ -134,7 +135,7 @@ __device__ __forceinline__ void decode_q5_pair(const uint32_t (&w)[TC_PAIR_WORDS
 }
 
 // Raw Q8_0 pair -> codes with the sign bit flipped (u = q + 128) and scales.
-__device__ __forceinline__ void decode_q8_pair(const uint32_t (&w)[TC_PAIR_WORDS], uint32_t (&c0)[8], uint32_t (&c1)[8],
+__device__ __forceinline__ void decode_q8_pair(const uint32_t (&w)[TP_PAIR_WORDS], uint32_t (&c0)[8], uint32_t (&c1)[8],
                                                float &d0, float &d1) {
     d0 = half_bits_to_float(w[0]);
     d1 = half_bits_to_float(w[8] >> 16);
@@ -145,226 +146,301 @@ __device__ __forceinline__ void decode_q8_pair(const uint32_t (&w)[TC_PAIR_WORDS
     }
 }
 
-template <bool OPROJ>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
+// tcgen05.ld of 8 / 16 consecutive fp32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *v) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Two fp32 lanes at once (each lane rounded as the scalar operation).
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
+}
+
+template <bool OPROJ, int NT>
+__global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, int S) {
+    static_assert(NT == 16 || NT == 32 || NT == 64, "MMA N");
+    constexpr int TMEM_COLS = TW_NTM * TP_BPS * NT;  // 128, 256 or 512: a power of two
+    constexpr int CW = NT / 2;                       // columns per consumer warp
     extern __shared__ __align__(1024) uint8_t smem[];
-    const TcSmem L = tc_smem();
+    const TpSmem L = tp_smem();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nb = OPROJ ? a.H * a.hd / QK : a.D / QK;
-    const int nst = nb / TC_BPS;
+    const int nst = nb / TP_BPS;
     const int QD = a.H * a.hd, KD = a.KV * a.hd;
-    const int R0 = blockIdx.x * TC_M;  // first global row of the tile
-    const int s0 = blockIdx.y * TC_N;  // first sequence
+    const int tile = blockIdx.x, split = blockIdx.y, g = blockIdx.z;
+    const int G = img_groups(a.B);
+    const int R0 = tile * TP_M;  // first global row of the tile
+    const int s0 = g * IMG_SEQ;  // first sequence
+    const int k0 = static_cast<int>(static_cast<long long>(split) * nst / S);
+    const int k1 = static_cast<int>(static_cast<long long>(split + 1) * nst / S);
+    const int T = k1 - k0;  // >= 1: S <= nst
     // the tile's matrix (a tile never straddles Q / K / V)
     int kind = 4;  // 0 = Q, 1 = K, 2 = V, 4 = O
     const uint8_t *W = a.wo;
-    int rbase = R0;
+    int rbase = R0, mrows = a.D;
     if (!OPROJ) {
         if (R0 < QD) {
             kind = 0;
             W = a.wq;
+            mrows = QD;
         } else if (R0 < QD + KD) {
             kind = 1;
             W = a.wk;
             rbase = R0 - QD;
+            mrows = KD;
         } else {
             kind = 2;
             W = a.wv;
             rbase = R0 - QD - KD;
+            mrows = KD;
         }
     }
     const bool wq8 = kind == 2;
+    const int pb = wq8 ? 2 * Q8B : 2 * Q5B;  // bytes per pair of blocks
     const size_t rb = static_cast<size_t>(nb) * (wq8 ? Q8B : Q5B);
-    const uint8_t *xq = OPROJ ? a.aq8 : a.xq8;  // Q8_0 blocks of the activation rows [B][nb]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bar);
+    const uint8_t *img = OPROJ ? a.aimg : a.ximg;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
+    uint64_t *a_full = bars, *a_empty = bars + TW_NA;
+    uint64_t *b_full = bars + 2 * TW_NA, *b_empty = b_full + TW_NB;
+    uint64_t *tm_full = b_empty + TW_NB, *tm_empty = tm_full + TW_NTM;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem);
-    const __half2 wbias = __half2half2(__float2half(wq8 ? 1152.0f : 1040.0f));
-    const __half2 xbias = __half2half2(__float2half(1152.0f));
+    auto a_tile = [&](int i) { return smem + L.a + static_cast<size_t>(i) * TP_A_BYTES; };
+    auto dw_of = [&](int i) { return reinterpret_cast<float *>(smem + L.dw + static_cast<size_t>(i) * TP_DW_BYTES); };
+    auto b_stage = [&](int i) { return smem + L.b + static_cast<size_t>(i) * IMG_STAGE_BYTES; };
 
-    // weight half of stage k into buffer k & 1, in two steps so that the
-    // loads are in flight while the previous stage is read back: load_w
-    // fetches the raw pairs of thread `tid` (TC_WPT pairs of a 256-thread
-    // sweep), decode_w writes them to the operand tile.
-    // Item `it` of a sweep is row (it & 7) + 8 (it >> 5), pair (it >> 3) & 3:
-    // the 8 threads of a quarter-warp write the 8 rows of one core matrix
-    // (distinct banks) and a warp reads 8 rows x 4 pairs (contiguous bytes).
-    constexpr int TC_WPT = TC_M * (TC_BPS / 2) / TC_THREADS;  // 2
-    auto load_w = [&](int k, uint32_t (&raw)[TC_WPT][TC_PAIR_WORDS]) {
-#pragma unroll
-        for (int u = 0; u < TC_WPT; ++u) {
-            const int it = tid + u * TC_THREADS;
-            const int r = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
-            const int blk = k * TC_BPS + 2 * p;
-            load_pair(W + static_cast<size_t>(rbase + r) * rb + static_cast<size_t>(blk) * (wq8 ? Q8B : Q5B), wq8,
-                      true, raw[u]);
-        }
-    };
-    auto decode_w = [&](int k, const uint32_t (&raw)[TC_WPT][TC_PAIR_WORDS]) {
-        uint8_t *tile = smem + buf(L.a, k);
-        float *dw = reinterpret_cast<float *>(smem + buf(L.dw, k));
-#pragma unroll
-        for (int u = 0; u < TC_WPT; ++u) {
-            const int it = tid + u * TC_THREADS;
-            const int r = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
-            uint32_t c0[8], c1[8];
-            float d0, d1;
-            if (wq8)
-                decode_q8_pair(raw[u], c0, c1, d0, d1);
-            else
-                decode_q5_pair(raw[u], c0, c1, d0, d1);
-            put_block(tile, r, 2 * p, c0, wbias);
-            put_block(tile, r, 2 * p + 1, c1, wbias);
-            dw[(2 * p) * TC_DWS + r] = d0;
-            dw[(2 * p + 1) * TC_DWS + r] = d1;
-        }
-    };
-    // activation half of stage k (after the wait on the preceding grid);
-    // scales stored block-major, dx[j][sequence]
-    auto convert_x = [&](int k) {
-        uint8_t *tile = smem + buf(L.b, k);
-        float *dx = reinterpret_cast<float *>(smem + buf(L.dx, k));
-        const int it = tid;
-        if (it < TC_N * (TC_BPS / 2)) {
-            const int sl = (it & 7) + 8 * (it >> 5), p = (it >> 3) & 3;
-            const int s = s0 + sl;
-            uint32_t c0[8], c1[8];
-            float d0 = 0.0f, d1 = 0.0f;
-            if (s < a.B) {
-                const int blk = k * TC_BPS + 2 * p;
-                uint32_t w[TC_PAIR_WORDS];
-                load_pair(xq + (static_cast<size_t>(s) * nb + blk) * Q8B, true, false, w);
-                decode_q8_pair(w, c0, c1, d0, d1);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) c0[i] = c1[i] = 0x80808080u;  // zero codes
-            }
-            put_block(tile, sl, 2 * p, c0, xbias);
-            put_block(tile, sl, 2 * p + 1, c1, xbias);
-            dx[(2 * p) * TC_N + sl] = d0;
-            dx[(2 * p + 1) * TC_N + sl] = d1;
-        }
-    };
-    auto issue_mma = [&](int k, uint32_t taddr) {  // thread 0
-        const uint32_t abase = sptr(smem + buf(L.a, k)), bbase = sptr(smem + buf(L.b, k));
-        const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(TC_N >> 3) << 17) |
-                               (static_cast<uint32_t>(TC_M >> 4) << 24);
-#pragma unroll
-        for (int j = 0; j < TC_BPS; ++j)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint64_t ad = tc_desc(abase + (4 * j + 2 * h) * 128);
-                const uint64_t bd = tc_desc(bbase + (4 * j + 2 * h) * 128);
-                asm volatile(
-                    "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                    "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(taddr + j * TC_N),
-                    "l"(ad), "l"(bd), "r"(idesc), "r"(h)
-                    : "memory");
-            }
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sptr(bar))
-                     : "memory");
-    };
-
-    // ---- prologue: the tile's weight rows (contiguous) into L2, barrier,
-    // TMEM, the first stage's weights before the wait
-    if (warp == 1) {
-        const size_t bytes = static_cast<size_t>(TC_M) * rb;
-        const uint8_t *base = W + static_cast<size_t>(rbase) * rb;
-        for (size_t o = static_cast<size_t>(lane) * 65536; o < bytes; o += 32 * 65536)
-            prefetch_l2(base + o, static_cast<uint32_t>(bytes - o < 65536 ? bytes - o : 65536));
-    }
+    // ---- setup: barriers, TMEM (the MMA warp), the producers' first loads
     if (tid == 0) {
-        mbar_init(bar, 1);
+        for (int i = 0; i < TW_NA; ++i) {
+            mbar_init(a_full + i, TW_PROD);
+            mbar_init(a_empty + i, TW_CONS);
+        }
+        for (int i = 0; i < TW_NB; ++i) {
+            mbar_init(b_full + i, 1);
+            mbar_init(b_empty + i, TW_CONS);
+        }
+        for (int i = 0; i < TW_NTM; ++i) {
+            mbar_init(tm_full + i, 1);
+            mbar_init(tm_empty + i, TW_CONS);
+        }
         fence_mbar_init();
     }
-    if (warp == 0) {
+    if (warp == TW_MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sptr(tmem_slot)),
-                     "r"(TC_TMEM_COLS)
+                     "r"(TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    uint32_t raw[TC_WPT][TC_PAIR_WORDS];
-    load_w(0, raw);
-    decode_w(0, raw);
     pdl_trigger();
-    pdl_wait();  // the activation blocks are ready
-    convert_x(0);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t taddr = *tmem_slot;
-    if (tid == 0) issue_mma(0, taddr);
 
-    // Every warp reads back half of each stage's blocks: warps w and w + 4
-    // share TMEM lanes 32 (w % 4) .. + 31 (the tile rows), blocks
-    // jh .. jh + 3.  Their two partial sums meet in the epilogue.
-    const int r = (warp & 3) * 32 + lane;
-    const int jh = (warp >> 2) * (TC_BPS / 2);
-    float acc[TC_N];
+    float *ep = reinterpret_cast<float *>(smem + L.a);  // [TP_M][NT + 1], after the main loop
+    constexpr int EPS = NT + 1;
+    // consumer warp w: TMEM lanes 32 (w % 4) .. + 31 (tile rows r), columns
+    // c0 .. c0 + NT/2 - 1 (sequences)
+    const int r = (warp & 3) * 32 + lane, c0 = (warp >> 2) * CW;
+    uint64_t acc[CW / 2];  // pairs of fp32 sums
 #pragma unroll
-    for (int i = 0; i < TC_N; ++i) acc[i] = 0.0f;
-    for (int k = 0; k < nst; ++k) {
-        const bool more = k + 1 < nst;
-        if (more) load_w(k + 1, raw);  // in flight during the read-back
-        if (!mbar_wait(bar, k & 1)) flag_error(a.status, FLAG_TIMEOUT);
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        {
-            const float *dw = reinterpret_cast<const float *>(smem + buf(L.dw, k)) + r;
-            const float4 *dx = reinterpret_cast<const float4 *>(smem + buf(L.dx, k));
+    for (int i = 0; i < CW / 2; ++i) acc[i] = 0;
+
+    if (warp >= TW_CONS && warp < TW_CONS + TW_PROD) {
+        // ---- producers: weight pairs -> fp16 A tiles and scales, up to
+        // TW_NA stages ahead of the read-back
+        const int pt = tid - 32 * TW_CONS, pw = pt >> 5;
+        const int cr = 16 * pw + (lane & 7) + 8 * (lane >> 4), cp = (lane >> 3) & 1;
+        const uint8_t *wrow = W + static_cast<size_t>(rbase + cr) * rb + static_cast<size_t>(cp) * pb;
+        if (pt < TP_M) {  // this CTA's weight bytes into L2, one row each
+            const size_t mend = static_cast<size_t>(mrows) * rb;
+            size_t lo = static_cast<size_t>(rbase + pt) * rb + static_cast<size_t>(k0) * (TP_BPS / 2) * pb;
+            size_t hi = lo + static_cast<size_t>(T) * (TP_BPS / 2) * pb;
+            lo &= ~static_cast<size_t>(15);
+            hi = (hi + 15) & ~static_cast<size_t>(15);
+            if (hi > mend) hi = mend;
+            if (hi > lo) prefetch_l2(W + lo, static_cast<uint32_t>(hi - lo));
+        }
+        const __half2 wbias = __half2half2(__float2half(wq8 ? 1152.0f : 1040.0f));
+        uint32_t rc[TP_PAIR_WORDS], rn[TP_PAIR_WORDS];
+        load_pair(wrow + static_cast<size_t>(k0) * (TP_BPS / 2) * pb, wq8, rc);
+        for (int t = 0; t < T; ++t) {
+            if (t + 1 < T) load_pair(wrow + static_cast<size_t>(k0 + t + 1) * (TP_BPS / 2) * pb, wq8, rn);
+            const int i = t % TW_NA, n = t / TW_NA;
+            if (n >= 1 && !mbar_wait(a_empty + i, (n - 1) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+            uint32_t c0[8], c1[8];
+            float d0, d1;
+            if (wq8)
+                decode_q8_pair(rc, c0, c1, d0, d1);
+            else
+                decode_q5_pair(rc, c0, c1, d0, d1);
+            uint8_t *tile_a = a_tile(i);
+            put_block(tile_a, cr, 2 * cp, c0, wbias);
+            put_block(tile_a, cr, 2 * cp + 1, c1, wbias);
+            float *dw = dw_of(i);
+            dw[(2 * cp) * TP_DWS + cr] = d0;
+            dw[(2 * cp + 1) * TP_DWS + cr] = d1;
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(a_full + i);
 #pragma unroll
-            for (int jj = 0; jj < TC_BPS / 2; ++jj) {
-                const int j = jh + jj;
-                uint32_t v[16];
+            for (int w = 0; w < TP_PAIR_WORDS; ++w) rc[w] = rn[w];
+        }
+    } else if (warp == TW_MMA_WARP) {
+        // ---- MMA warp: activation stages (bulk copies, TW_NB in flight)
+        // and the MMAs of each stage into its TMEM slot
+        if (lane == 0) {
+            pdl_wait();  // the activation image is ready
+            auto copy_b = [&](int t) {
+                const int i = t % TW_NB;
+                uint8_t *dst = b_stage(i);
+                const uint8_t *src = img + img_stage(G, k0 + t, g);
+                mbar_arrive_expect_tx(b_full + i, NT * (IMG_RG_BYTES / 8) + IMG_BPS * IMG_SEQ * 4);
+                bulk_g2s(dst, src, NT * (IMG_RG_BYTES / 8), b_full + i);
+                bulk_g2s(dst + IMG_CODE_BYTES, src + IMG_CODE_BYTES, IMG_BPS * IMG_SEQ * 4, b_full + i);
+            };
+            for (int t = 0; t < T && t < TW_NB; ++t) copy_b(t);
+            const uint32_t idesc =
+                (1u << 4) | (static_cast<uint32_t>(NT >> 3) << 17) | (static_cast<uint32_t>(TP_M >> 4) << 24);
+            for (int t = 0; t < T; ++t) {
+                const int ia = t % TW_NA, ib = t % TW_NB, im = t % TW_NTM;
+                bool ok = mbar_wait(a_full + ia, (t / TW_NA) & 1);
+                ok = mbar_wait(b_full + ib, (t / TW_NB) & 1) && ok;
+                if (t >= TW_NTM) ok = mbar_wait(tm_empty + im, (t / TW_NTM - 1) & 1) && ok;
+                if (!ok) flag_error(a.status, FLAG_TIMEOUT);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t abase = sptr(a_tile(ia)), bbase = sptr(b_stage(ib));
+                const uint32_t dcol = taddr + im * TP_BPS * NT;
+#pragma unroll
+                for (int j = 0; j < TP_BPS; ++j)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint64_t ad = tp_desc(abase + (4 * j + 2 * h) * 128);
+                        const uint64_t bd = tp_desc(bbase + (4 * j + 2 * h) * 128);
+                        asm volatile(
+                            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dcol + j * NT),
+                            "l"(ad), "l"(bd), "r"(idesc), "r"(h)
+                            : "memory");
+                    }
                 asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-                    "[%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-                      "=r"(v[14]), "=r"(v[15])
-                    : "r"(taddr + (static_cast<uint32_t>((warp & 3) * 32) << 16) + j * TC_N)
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sptr(tm_full + im))
                     : "memory");
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                const float dwv = dw[j * TC_DWS];
-#pragma unroll
-                for (int q4 = 0; q4 < TC_N / 4; ++q4) {
-                    const float4 d4 = dx[j * (TC_N / 4) + q4];
-                    acc[4 * q4 + 0] = fmaf(__uint_as_float(v[4 * q4 + 0]), dwv * d4.x, acc[4 * q4 + 0]);
-                    acc[4 * q4 + 1] = fmaf(__uint_as_float(v[4 * q4 + 1]), dwv * d4.y, acc[4 * q4 + 1]);
-                    acc[4 * q4 + 2] = fmaf(__uint_as_float(v[4 * q4 + 2]), dwv * d4.z, acc[4 * q4 + 2]);
-                    acc[4 * q4 + 3] = fmaf(__uint_as_float(v[4 * q4 + 3]), dwv * d4.w, acc[4 * q4 + 3]);
+                // stage t - 1 read back: its activation slot takes stage t + TW_NB - 1
+                if (t >= 1 && t + TW_NB - 1 < T) {
+                    if (!mbar_wait(b_empty + (t - 1) % TW_NB, ((t - 1) / TW_NB) & 1))
+                        flag_error(a.status, FLAG_TIMEOUT);
+                    copy_b(t + TW_NB - 1);
                 }
             }
         }
-        if (more) {  // stage k + 1 into the buffers stage k - 1 used
-            decode_w(k + 1, raw);
-            convert_x(k + 1);
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+    } else {
+        // ---- consumers: fold each block's exact dots in with its two scales
+        for (int t = 0; t < T; ++t) {
+            const int ia = t % TW_NA, ib = t % TW_NB, im = t % TW_NTM;
+            // the stage's MMAs are done; the scales written by the producers
+            // and by the bulk copy are acquired from their own barriers (whose
+            // next phases need this stage's release, so they are current)
+            bool ok = mbar_wait(tm_full + im, (t / TW_NTM) & 1);
+            ok = mbar_wait(a_full + ia, (t / TW_NA) & 1) && ok;
+            ok = mbar_wait(b_full + ib, (t / TW_NB) & 1) && ok;
+            if (!ok) flag_error(a.status, FLAG_TIMEOUT);
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const float *dw = dw_of(ia) + r;
+            const float *dx = reinterpret_cast<const float *>(b_stage(ib) + IMG_CODE_BYTES);
+            const uint32_t base = taddr + (static_cast<uint32_t>((warp & 3) * 32) << 16) + im * TP_BPS * NT + c0;
+            constexpr int CH = CW < 16 ? CW : 16;  // columns per TMEM load
+#pragma unroll
+            for (int j = 0; j < TP_BPS; ++j) {
+                const float dwv = dw[j * TP_DWS];
+                const uint64_t dw2 = f2_pack(__float_as_uint(dwv), __float_as_uint(dwv));
+                const uint64_t *dx2 = reinterpret_cast<const uint64_t *>(dx + j * IMG_SEQ + c0);
+#pragma unroll
+                for (int c = 0; c < CW / CH; ++c) {
+                    uint32_t v[CH];
+                    if constexpr (CH == 16)
+                        tmem_ld16(base + j * NT + CH * c, v);
+                    else
+                        tmem_ld8(base + j * NT + CH * c, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int p = 0; p < CH / 2; ++p)
+                        acc[c * CH / 2 + p] = f2_fma(f2_pack(v[2 * p], v[2 * p + 1]),
+                                                     f2_mul(dw2, dx2[c * CH / 2 + p]), acc[c * CH / 2 + p]);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(tm_empty + im);
+                mbar_arrive(a_empty + ia);
+                mbar_arrive(b_empty + ib);
+            }
         }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();  // stage k read back, stage k + 1 converted
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (tid == 0 && more) issue_mma(k + 1, taddr);
     }
-
-    // ---- epilogue through shared memory
-    float *ep = reinterpret_cast<float *>(smem + L.ep);
-    if (warp >= 4) {
-#pragma unroll
-        for (int s = 0; s < TC_N; ++s) ep[r * (TC_N + 1) + s] = acc[s];
-    }
-    __syncthreads();
-    if (warp < 4) {
-#pragma unroll
-        for (int s = 0; s < TC_N; ++s) ep[r * (TC_N + 1) + s] += acc[s];
-    }
+    // Every MMA has completed (the consumers saw the last one) and every A
+    // tile has been read: the A tiles take the sums.
+    pdl_wait();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
+    if (warp < TW_CONS) {
+#pragma unroll
+        for (int p = 0; p < CW / 2; ++p) {
+            ep[r * EPS + c0 + 2 * p] = __uint_as_float(static_cast<uint32_t>(acc[p]));
+            ep[r * EPS + c0 + 2 * p + 1] = __uint_as_float(static_cast<uint32_t>(acc[p] >> 32));
+        }
+    }
+    __syncthreads();  // the sums are in ep
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TC_TMEM_COLS));
+    if (warp == TW_MMA_WARP)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS));
+
+    if (S > 1) {
+        // publish this split's tile; the last CTA of the tile sums all splits
+        float *part = a.proj_part + (static_cast<size_t>(tile) * G + g) * S * (TP_M * NT);
+        for (int i = tid; i < TP_M * NT; i += TW_THREADS)
+            part[static_cast<size_t>(split) * (TP_M * NT) + i] = ep[(i / NT) * EPS + (i % NT)];
+        __threadfence();
+        __syncthreads();
+        int *tk = reinterpret_cast<int *>(smem + L.ticket);
+        if (tid == 0) *tk = atomicAdd(a.tickets + (OPROJ ? a.tickets_o : 0) + tile * G + g, 1);
+        __syncthreads();
+        if (*tk != S - 1) return;
+        __threadfence();
+        for (int i = tid; i < TP_M * NT; i += TW_THREADS) {
+            float v = 0.0f;
+            for (int sp = 0; sp < S; ++sp) v += __ldcg(part + static_cast<size_t>(sp) * (TP_M * NT) + i);
+            ep[(i / NT) * EPS + (i % NT)] = v;
+        }
+        __syncthreads();
+    }
+
+    // ---- epilogue
     const int half = a.hd >> 1;
     if (kind == 0 || kind == 1) {  // RoPE pairs (l, l + hd/2) of the tile's heads
-        for (int it = tid; it < (TC_M / 2) * TC_N; it += TC_THREADS) {
-            const int pr = it / TC_N, sl = it - pr * TC_N;
+        for (int it = tid; it < (TP_M / 2) * NT; it += TW_THREADS) {
+            const int pr = it / NT, sl = it - pr * NT;
             const int s = s0 + sl;
             if (s >= a.B) continue;
             const int pos = a.d_pos[s];
@@ -375,8 +451,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
             const int l = (pr / half) * a.hd + (pr % half);  // first row of the pair in the tile
             const int ra = rbase + l, rbb = ra + half;
             const float *bias = kind == 0 ? a.bq : a.bk;
-            const float A = ep[l * (TC_N + 1) + sl] + (bias ? bias[ra] : 0.0f);
-            const float B = ep[(l + half) * (TC_N + 1) + sl] + (bias ? bias[rbb] : 0.0f);
+            const float A = ep[l * EPS + sl] + (bias ? bias[ra] : 0.0f);
+            const float B = ep[(l + half) * EPS + sl] + (bias ? bias[rbb] : 0.0f);
             const int head = ra / a.hd, i = ra - head * a.hd;
             const float c = a.rope_cos[static_cast<size_t>(pos) * half + i];
             const float sn = a.rope_sin[static_cast<size_t>(pos) * half + i];
@@ -392,8 +468,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
             }
         }
     } else {
-        for (int it = tid; it < TC_M * TC_N; it += TC_THREADS) {
-            const int l = it / TC_N, sl = it - l * TC_N;
+        for (int it = tid; it < TP_M * NT; it += TW_THREADS) {
+            const int l = it / NT, sl = it - l * NT;
             const int s = s0 + sl;
             if (s >= a.B) continue;
             const int pos = a.d_pos[s];
@@ -401,15 +477,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
                 flag_error(a.status, FLAG_RANGE);
                 continue;
             }
-            const int r = rbase + l;
-            const float v = ep[l * (TC_N + 1) + sl];
+            const int rr = rbase + l;
+            const float v = ep[l * EPS + sl];
             if (kind == 4) {
-                a.out[static_cast<size_t>(s) * a.D + r] =
-                    (v + (a.bo ? a.bo[r] : 0.0f)) + a.residual[static_cast<size_t>(s) * a.D + r];
+                a.out[static_cast<size_t>(s) * a.D + rr] =
+                    (v + (a.bo ? a.bo[rr] : 0.0f)) + a.residual[static_cast<size_t>(s) * a.D + rr];
             } else {
-                const int h = r / a.hd;
-                a.v_caches[s][(static_cast<size_t>(h) * a.C + pos) * a.hd + (r - h * a.hd)] =
-                    v + (a.bv ? a.bv[r] : 0.0f);
+                const int h = rr / a.hd;
+                a.v_caches[s][(static_cast<size_t>(h) * a.C + pos) * a.hd + (rr - h * a.hd)] =
+                    v + (a.bv ? a.bv[rr] : 0.0f);
             }
         }
     }
@@ -417,19 +493,57 @@ __global__ void __launch_bounds__(TC_THREADS, 1) k_rows_tc(const BatchArgs a) {
 
 bool batched_tc_ok(int D, int H, int KV, int hd) {
     const int QD = H * hd, KD = KV * hd;
-    return (hd == 64 || hd == 128) && D % TC_M == 0 && QD % TC_M == 0 && KD % TC_M == 0 &&
-           (D / QK) % TC_BPS == 0 && (QD / QK) % TC_BPS == 0 && tc_smem().total <= device_info().smem_optin;
+    return (hd == 64 || hd == 128) && D % TP_M == 0 && QD % TP_M == 0 && KD % TP_M == 0 &&
+           tp_smem().total <= device_info().smem_optin;
 }
 
-int launch_rows_tc(const BatchArgs &a0, bool oproj, cudaStream_t s, bool pdl) {
-    BatchArgs a = a0;
-    const int rows = oproj ? a.D : (a.H + 2 * a.KV) * a.hd;
-    const dim3 grid(rows / TC_M, (a.B + TC_N - 1) / TC_N);
-    const void *fn = oproj ? reinterpret_cast<const void *>(k_rows_tc<true>)
-                           : reinterpret_cast<const void *>(k_rows_tc<false>);
-    ensure_smem(fn, tc_smem().total);
-    void *args[] = {&a};
-    return launch(fn, grid, dim3(TC_THREADS), tc_smem().total, s, pdl, args) == cudaSuccess ? 0 : -5;
+static int tp_nt(int B) { return B > 32 ? 64 : B > 16 ? 32 : 16; }
+
+TpPlan tp_plan(int B, int D, int H, int KV, int hd, bool with_device) {
+    TpPlan p{};
+    const int G = img_groups(B);
+    const int nsm = with_device ? device_info().num_sms : 0;
+    const int nt = tp_nt(B);
+    const int tiles[2] = {(H + 2 * KV) * hd / TP_M, D / TP_M};
+    const int nst[2] = {D / QK / TP_BPS, H * hd / QK / TP_BPS};
+    size_t part = 0;
+    for (int i = 0; i < 2; ++i) {
+        const int smax = nst[i] < TP_MAX_SPLITS ? nst[i] : TP_MAX_SPLITS;
+        int S = nsm / (tiles[i] * G);
+        p.splits[i] = S < 1 ? 1 : S > smax ? smax : S;
+        // scratch for the partial tiles: sized for the most splits (the
+        // same on every device)
+        const size_t bytes = static_cast<size_t>(tiles[i]) * G * smax * TP_M * nt * 4;
+        part = bytes > part ? bytes : part;
+    }
+    p.part_bytes = part;
+    p.tickets_o = tiles[0] * G;
+    p.tickets = tiles[0] * G + tiles[1] * G;
+    return p;
+}
+
+template <bool OPROJ, int NT>
+static cudaError_t launch_tp(const BatchArgs &a, int S, cudaStream_t s, bool pdl) {
+    const int rows = OPROJ ? a.D : (a.H + 2 * a.KV) * a.hd;
+    const dim3 grid(rows / TP_M, S, img_groups(a.B));
+    const void *fn = reinterpret_cast<const void *>(k_proj_tc<OPROJ, NT>);
+    ensure_smem(fn, tp_smem().total);
+    BatchArgs ac = a;
+    int Sc = S;
+    void *args[] = {&ac, &Sc};
+    return launch(fn, grid, dim3(TW_THREADS), tp_smem().total, s, pdl, args);
+}
+
+int launch_rows_tc(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl) {
+    const TpPlan p = tp_plan(a.B, a.D, a.H, a.KV, a.hd, true);
+    const int S = p.splits[oproj ? 1 : 0];
+    cudaError_t e;
+    switch (tp_nt(a.B)) {
+        case 16: e = oproj ? launch_tp<true, 16>(a, S, s, pdl) : launch_tp<false, 16>(a, S, s, pdl); break;
+        case 32: e = oproj ? launch_tp<true, 32>(a, S, s, pdl) : launch_tp<false, 32>(a, S, s, pdl); break;
+        default: e = oproj ? launch_tp<true, 64>(a, S, s, pdl) : launch_tp<false, 64>(a, S, s, pdl); break;
+    }
+    return e == cudaSuccess ? 0 : -5;
 }
 
 }  // namespace ck

@@ -42,6 +42,11 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// Arrive once on the barrier (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sptr(bar)) : "memory");
+}
+
 // Arrive once on the barrier and add `bytes` to the transactions it expects.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sptr(bar)), "r"(bytes) : "memory");
@@ -149,6 +154,55 @@ __host__ __device__ constexpr int xq_chunks(int nb) { return 2 * nb + nb / 8 + 1
 // fp32 scales, then nb int32 code sums), rounded up to 16.
 __host__ __device__ constexpr size_t xpack_bytes(int nb) {
     return (static_cast<size_t>(xq_chunks(nb)) * 16 + static_cast<size_t>(nb) * 8 + 15) / 16 * 16;
+}
+
+// ---------------------------------------------------------------------------
+// Operand image of a batch of Q8_0 activation rows for the tensor-core
+// projections.  Rows (sequences) go in groups of IMG_SEQ, blocks in stages of
+// IMG_BPS (128 codes).  Stage k of group g holds 16 KB of codes as fp16 in
+// the MMA operand layout (core matrices of 8 rows x 8 codes = 128 bytes, 16
+// of them along K per 8-row group, 8-row groups IMG_RG_BYTES apart), then the
+// IMG_BPS x IMG_SEQ block scales (fp32, [block][row]).  A CTA takes a stage's
+// rows with one bulk copy of the codes and one of the scales.
+// ---------------------------------------------------------------------------
+constexpr int IMG_SEQ = 64;
+constexpr int IMG_BPS = 4;
+constexpr int IMG_KG = IMG_BPS * 4;                                      // 8-code groups along K
+constexpr int IMG_RG_BYTES = IMG_KG * 128;                               // one 8-row group
+constexpr int IMG_CODE_BYTES = IMG_SEQ / 8 * IMG_RG_BYTES;               // 16 KB
+constexpr int IMG_STAGE_BYTES = IMG_CODE_BYTES + IMG_BPS * IMG_SEQ * 4;  // + 1 KB of scales
+__host__ __device__ constexpr int img_groups(int B) { return (B + IMG_SEQ - 1) / IMG_SEQ; }
+__host__ __device__ constexpr size_t img_bytes(int nb, int B) {
+    return static_cast<size_t>(nb / IMG_BPS) * img_groups(B) * IMG_STAGE_BYTES;
+}
+__host__ __device__ constexpr size_t img_stage(int G, int k, int g) {
+    return (static_cast<size_t>(k) * G + g) * IMG_STAGE_BYTES;
+}
+// The 16 bytes holding codes 8e .. 8e + 7 of block b of row s.
+__host__ __device__ constexpr size_t img_code_off(int G, int s, int b, int e) {
+    return img_stage(G, b / IMG_BPS, s / IMG_SEQ) + static_cast<size_t>(((s % IMG_SEQ) >> 3) * IMG_RG_BYTES) +
+           static_cast<size_t>(((b % IMG_BPS) * 4 + e) * 128 + (s & 7) * 16);
+}
+__host__ __device__ constexpr size_t img_d_off(int G, int s, int b) {
+    return img_stage(G, b / IMG_BPS, s / IMG_SEQ) + IMG_CODE_BYTES +
+           static_cast<size_t>((b % IMG_BPS) * IMG_SEQ + s % IMG_SEQ) * 4;
+}
+// Eight signed Q8_0 codes (two words, element order) as eight fp16 values,
+// exactly: byte u = q + 128 becomes the fp16 1024 + u, minus 1152.
+__device__ __forceinline__ uint4 q8_codes_to_half8(uint32_t w0, uint32_t w1) {
+    const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
+    uint32_t h[4];
+    const uint32_t c[2] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t lo = __byte_perm(c[i], 0x64646464u, 0x5140);
+        const uint32_t hi = __byte_perm(c[i], 0x64646464u, 0x7362);
+        const __half2 a = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
+        const __half2 b = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
+        h[2 * i] = *reinterpret_cast<const uint32_t *>(&a);
+        h[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&b);
+    }
+    return make_uint4(h[0], h[1], h[2], h[3]);
 }
 
 struct XRow {

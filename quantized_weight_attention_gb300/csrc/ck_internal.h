@@ -81,11 +81,25 @@ struct BatchArgs {
     uint8_t *xpack;  // [B] packed rows of the normed inputs
     uint8_t *apack;  // [B] packed rows of the attention outputs
     uint8_t *aq8;    // [B][H*hd/32] Q8_0 blocks of the attention outputs
+    uint8_t *ximg;   // tensor-core operand image of the normed inputs (img_bytes(D/32, B)), or null
+    uint8_t *aimg;   // the same for the attention outputs (img_bytes(H*hd/32, B))
+    float *proj_part;  // tensor-core projections: partial tiles of the K splits
+    int *tickets;      // per tile: K splits finished (QKV tiles, then O tiles from tickets_o)
+    int tickets_o, n_tickets;
     unsigned *status;
 };
 bool batched_shape_ok(int D, int H, int hd);
-// Tensor-core projections (ck_batched_tc.cu): shapes they take, and launch.
+// Tensor-core projections (ck_batched_tc.cu): shapes they take, their plan
+// (K splits of the QKV and O launches, scratch of the partial tiles, tile
+// tickets) and launch.  Without the device the splits are 1 and only the
+// sizes, which do not depend on it, are meaningful.
 bool batched_tc_ok(int D, int H, int KV, int hd);
+struct TpPlan {
+    int splits[2];
+    size_t part_bytes;
+    int tickets_o, tickets;
+};
+TpPlan tp_plan(int B, int D, int H, int KV, int hd, bool with_device);
 int launch_rows_tc(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 int launch_norm_pack(const BatchArgs &a, cudaStream_t s, bool pdl);
 int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
@@ -107,6 +121,8 @@ struct AttnArgs {
     float *out;               // [B][H*hd] fp32 attention output
     uint8_t *out_q8;          // [B][H*hd/32] Q8_0 blocks, or null
     uint8_t *out_pack;        // [B] packed rows of those blocks (xpack_bytes each), or null
+    uint8_t *out_img;         // tensor-core operand image of those blocks (img_* layout), or null
+    int img_groups;           // its sequence groups: img_groups(B)
     const void *l2_prefetch;  // optional: bytes the next kernel reads, pulled into L2
     size_t l2_prefetch_bytes;
     unsigned *status;
