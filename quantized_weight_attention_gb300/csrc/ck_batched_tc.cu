@@ -404,23 +404,30 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
     pdl_wait();
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (warp < TW_CONS) {
-#pragma unroll
-        for (int p = 0; p < CW / 2; ++p) {
-            ep[r * EPS + c0 + 2 * p] = __uint_as_float(static_cast<uint32_t>(acc[p]));
-            ep[r * EPS + c0 + 2 * p + 1] = __uint_as_float(static_cast<uint32_t>(acc[p] >> 32));
-        }
-    }
-    __syncthreads();  // the sums are in ep
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == TW_MMA_WARP)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(TMEM_COLS));
-
-    if (S > 1) {
-        // publish this split's tile; the last CTA of the tile sums all splits
+    if (S == 1) {
+        if (warp < TW_CONS) {
+#pragma unroll
+            for (int p = 0; p < CW / 2; ++p) {
+                ep[r * EPS + c0 + 2 * p] = __uint_as_float(static_cast<uint32_t>(acc[p]));
+                ep[r * EPS + c0 + 2 * p + 1] = __uint_as_float(static_cast<uint32_t>(acc[p] >> 32));
+            }
+        }
+    } else {
+        // publish this split's tile [TP_M][NT] straight from the registers;
+        // the last CTA of the tile sums all splits in split order
         float *part = a.proj_part + (static_cast<size_t>(tile) * G + g) * S * (TP_M * NT);
-        for (int i = tid; i < TP_M * NT; i += TW_THREADS)
-            part[static_cast<size_t>(split) * (TP_M * NT) + i] = ep[(i / NT) * EPS + (i % NT)];
+        if (warp < TW_CONS) {
+            float4 *dst = reinterpret_cast<float4 *>(part + static_cast<size_t>(split) * (TP_M * NT) + r * NT + c0);
+#pragma unroll
+            for (int p = 0; p < CW / 4; ++p)
+                dst[p] = make_float4(__uint_as_float(static_cast<uint32_t>(acc[2 * p])),
+                                     __uint_as_float(static_cast<uint32_t>(acc[2 * p] >> 32)),
+                                     __uint_as_float(static_cast<uint32_t>(acc[2 * p + 1])),
+                                     __uint_as_float(static_cast<uint32_t>(acc[2 * p + 1] >> 32)));
+        }
         __threadfence();
         __syncthreads();
         int *tk = reinterpret_cast<int *>(smem + L.ticket);
@@ -428,64 +435,118 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
         __syncthreads();
         if (*tk != S - 1) return;
         __threadfence();
-        for (int i = tid; i < TP_M * NT; i += TW_THREADS) {
-            float v = 0.0f;
-            for (int sp = 0; sp < S; ++sp) v += __ldcg(part + static_cast<size_t>(sp) * (TP_M * NT) + i);
-            ep[(i / NT) * EPS + (i % NT)] = v;
+        // TP_M * NT / 4 float4 per split; thread i takes float4 i, i + 512,
+        // ... with every split's loads in flight before the sums
+        constexpr int NV = TP_M * NT / 4 / 512;  // 1, 2 or 4
+        if (tid < 512) {
+            float4 sum[NV];
+#pragma unroll
+            for (int u = 0; u < NV; ++u) sum[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            const float4 *src = reinterpret_cast<const float4 *>(part);
+            for (int sp0 = 0; sp0 < S; sp0 += 4) {
+                float4 v[4][NV];
+#pragma unroll
+                for (int d = 0; d < 4; ++d)
+#pragma unroll
+                    for (int u = 0; u < NV; ++u)
+                        if (sp0 + d < S) v[d][u] = __ldcg(src + static_cast<size_t>(sp0 + d) * (TP_M * NT / 4) + tid + 512 * u);
+#pragma unroll
+                for (int d = 0; d < 4; ++d)
+#pragma unroll
+                    for (int u = 0; u < NV; ++u)
+                        if (sp0 + d < S) {
+                            sum[u].x += v[d][u].x;
+                            sum[u].y += v[d][u].y;
+                            sum[u].z += v[d][u].z;
+                            sum[u].w += v[d][u].w;
+                        }
+            }
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const int e = 4 * (tid + 512 * u), row = e / NT, col = e % NT;
+                float *o = ep + row * EPS + col;
+                o[0] = sum[u].x;
+                o[1] = sum[u].y;
+                o[2] = sum[u].z;
+                o[3] = sum[u].w;
+            }
         }
-        __syncthreads();
     }
+    __syncthreads();  // the tile's sums are in ep
 
-    // ---- epilogue
+    // ---- epilogue: thread -> sequence column sl = tid % NT and a group of
+    // rows; the sequence's position (and cache rows) once, every load of the
+    // thread's rows issued before any is used
+    constexpr int NGRP = 512 / NT;  // row groups
+    if (tid >= 512) return;
+    const int sl = tid % NT, grp = tid / NT;
+    const int s = s0 + sl;
+    if (s >= a.B) return;
+    const int pos = a.d_pos[s];
+    if (pos < 0 || pos >= a.C) {
+        flag_error(a.status, FLAG_RANGE);
+        return;
+    }
     const int half = a.hd >> 1;
     if (kind == 0 || kind == 1) {  // RoPE pairs (l, l + hd/2) of the tile's heads
-        for (int it = tid; it < (TP_M / 2) * NT; it += TW_THREADS) {
-            const int pr = it / NT, sl = it - pr * NT;
-            const int s = s0 + sl;
-            if (s >= a.B) continue;
-            const int pos = a.d_pos[s];
-            if (pos < 0 || pos >= a.C) {
-                flag_error(a.status, FLAG_RANGE);
-                continue;
-            }
-            const int l = (pr / half) * a.hd + (pr % half);  // first row of the pair in the tile
+        constexpr int PP = (TP_M / 2) / NGRP;  // pairs per thread
+        const float *bias = kind == 0 ? a.bq : a.bk;
+        float cv[PP], sv[PP], ba[PP], bb[PP];
+#pragma unroll
+        for (int u = 0; u < PP; ++u) {
+            const int pr = grp + NGRP * u;
+            const int l = (pr / half) * a.hd + (pr % half);
+            const int ra = rbase + l;
+            const int i = ra % a.hd;
+            cv[u] = a.rope_cos[static_cast<size_t>(pos) * half + i];
+            sv[u] = a.rope_sin[static_cast<size_t>(pos) * half + i];
+            ba[u] = bias ? bias[ra] : 0.0f;
+            bb[u] = bias ? bias[ra + half] : 0.0f;
+        }
+        float *krow = nullptr;
+        if (kind == 1) krow = a.k_caches[s];
+#pragma unroll
+        for (int u = 0; u < PP; ++u) {
+            const int pr = grp + NGRP * u;
+            const int l = (pr / half) * a.hd + (pr % half);
             const int ra = rbase + l, rbb = ra + half;
-            const float *bias = kind == 0 ? a.bq : a.bk;
-            const float A = ep[l * EPS + sl] + (bias ? bias[ra] : 0.0f);
-            const float B = ep[(l + half) * EPS + sl] + (bias ? bias[rbb] : 0.0f);
-            const int head = ra / a.hd, i = ra - head * a.hd;
-            const float c = a.rope_cos[static_cast<size_t>(pos) * half + i];
-            const float sn = a.rope_sin[static_cast<size_t>(pos) * half + i];
-            const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, sn));
-            const float B2 = __fadd_rn(__fmul_rn(A, sn), __fmul_rn(B, c));
+            const float A = ep[l * EPS + sl] + ba[u];
+            const float B = ep[(l + half) * EPS + sl] + bb[u];
+            const float A2 = __fsub_rn(__fmul_rn(A, cv[u]), __fmul_rn(B, sv[u]));
+            const float B2 = __fadd_rn(__fmul_rn(A, sv[u]), __fmul_rn(B, cv[u]));
             if (kind == 0) {
                 a.q[static_cast<size_t>(s) * QD + ra] = A2;
                 a.q[static_cast<size_t>(s) * QD + rbb] = B2;
             } else {
-                float *kr = a.k_caches[s] + (static_cast<size_t>(head) * a.C + pos) * a.hd;
+                const int head = ra / a.hd, i = ra - head * a.hd;
+                float *kr = krow + (static_cast<size_t>(head) * a.C + pos) * a.hd;
                 kr[i] = A2;
                 kr[i + half] = B2;
             }
         }
     } else {
-        for (int it = tid; it < TP_M * NT; it += TW_THREADS) {
-            const int l = it / NT, sl = it - l * NT;
-            const int s = s0 + sl;
-            if (s >= a.B) continue;
-            const int pos = a.d_pos[s];
-            if (pos < 0 || pos >= a.C) {
-                flag_error(a.status, FLAG_RANGE);
-                continue;
+        constexpr int RR = TP_M / NGRP;  // rows per thread
+        float xv[RR], bo[RR];  // O: residual and bias; V: bias
+#pragma unroll
+        for (int u = 0; u < RR; ++u) {
+            const int rr = rbase + grp + NGRP * u;
+            if (kind == 4) {
+                xv[u] = a.residual[static_cast<size_t>(s) * a.D + rr];
+                bo[u] = a.bo ? a.bo[rr] : 0.0f;
+            } else {
+                xv[u] = a.bv ? a.bv[rr] : 0.0f;
             }
-            const int rr = rbase + l;
+        }
+        float *vrow = kind == 2 ? a.v_caches[s] : nullptr;
+#pragma unroll
+        for (int u = 0; u < RR; ++u) {
+            const int l = grp + NGRP * u, rr = rbase + l;
             const float v = ep[l * EPS + sl];
             if (kind == 4) {
-                a.out[static_cast<size_t>(s) * a.D + rr] =
-                    (v + (a.bo ? a.bo[rr] : 0.0f)) + a.residual[static_cast<size_t>(s) * a.D + rr];
+                a.out[static_cast<size_t>(s) * a.D + rr] = (v + bo[u]) + xv[u];
             } else {
                 const int h = rr / a.hd;
-                a.v_caches[s][(static_cast<size_t>(h) * a.C + pos) * a.hd + (rr - h * a.hd)] =
-                    v + (a.bv ? a.bv[rr] : 0.0f);
+                vrow[(static_cast<size_t>(h) * a.C + pos) * a.hd + (rr - h * a.hd)] = v + xv[u];
             }
         }
     }
