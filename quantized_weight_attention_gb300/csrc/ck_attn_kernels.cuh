@@ -485,12 +485,13 @@ __device__ __forceinline__ void combine_store(const AttnArgs &a, int b, int h, i
             qb[0] = static_cast<uint8_t>(dbits & 0xFF);
             qb[1] = static_cast<uint8_t>(dbits >> 8);
         }
-        if (a.out_img) {  // the block in the tensor-core operand image: one fp16 code per lane
+        if (a.out_img) {  // the block in the tensor-core operand image: one value per lane, hi and lo
             const int bq = h * (HD / 32) + blk;
-            const __half hq = __int2half_rn(q);
-            *reinterpret_cast<__half *>(a.out_img + img_code_off(a.img_groups, b, bq, lane >> 3) + (lane & 7) * 2) =
-                hq;
-            if (lane == 0) *reinterpret_cast<float *>(a.out_img + img_d_off(a.img_groups, b, bq)) = dq;
+            __half hi, lo;
+            if (!img_split(dq, q, hi, lo)) flag_error(a.status, FLAG_RANGE);
+            uint8_t *o = a.out_img + img_code_off(a.img_groups, b, bq, lane >> 3) + (lane & 7) * 2;
+            *reinterpret_cast<__half *>(o) = hi;
+            *reinterpret_cast<__half *>(o + IMG_CODE_BYTES) = lo;
         }
         if (a.out_pack) {  // the same block in the packed row the O-projection copies
             const int nbo = a.H * (HD / 32), bq = h * (HD / 32) + blk;

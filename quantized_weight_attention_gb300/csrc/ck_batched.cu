@@ -52,15 +52,21 @@ __global__ void __launch_bounds__(512) k_norm_pack(const BatchArgs a) {
     const int n16 = static_cast<int>(xpack_bytes(nb) / 16);
     int4 *dst = reinterpret_cast<int4 *>(a.xpack + static_cast<size_t>(s) * xpack_bytes(nb));
     for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = xr.q[i];
-    if (a.ximg) {  // the row in the tensor-core operand image: 8 codes per item, then the scales
+    if (a.ximg) {  // the row in the tensor-core operand image: 8 values per item, hi and lo parts
         const int G = img_groups(a.B);
+        bool in_range = true;
         for (int i = threadIdx.x; i < nb * 4; i += blockDim.x) {
             const int b = i >> 2, e = i & 3;
-            const uint32_t *w = reinterpret_cast<const uint32_t *>(&xr.q[xq_chunk(b, e >> 1)]) + (e & 1) * 2;
-            *reinterpret_cast<uint4 *>(a.ximg + img_code_off(G, s, b, e)) = q8_codes_to_half8(w[0], w[1]);
+            const int8_t *c = reinterpret_cast<const int8_t *>(&xr.q[xq_chunk(b, e >> 1)]) + (e & 1) * 8;
+            const float d = xr.d[b];
+            __align__(16) __half hi[8], lo[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) in_range = img_split(d, c[k], hi[k], lo[k]) && in_range;
+            uint8_t *o = a.ximg + img_code_off(G, s, b, e);
+            *reinterpret_cast<uint4 *>(o) = *reinterpret_cast<const uint4 *>(hi);
+            *reinterpret_cast<uint4 *>(o + IMG_CODE_BYTES) = *reinterpret_cast<const uint4 *>(lo);
         }
-        for (int b = threadIdx.x; b < nb; b += blockDim.x)
-            *reinterpret_cast<float *>(a.ximg + img_d_off(G, s, b)) = xr.d[b];
+        if (!in_range) flag_error(a.status, FLAG_RANGE);
     }
 }
 

@@ -1,13 +1,14 @@
 // Batched projections on the 5th-generation tensor cores (tcgen05, kind::f16).
 //
 // For B activation rows sharing one weight matrix the projection
-//   y[s][r] = sum_b d_w[r][b] * d_x[s][b] * isum[r][s][b]
-// is a dense contraction.  Codes are exact in fp16 (Q5_0: q - 16 in [-16, 15];
-// Q8_0: [-127, 127]), their products and 32-term block sums are exact in the
-// fp32 accumulator, so one MMA pair per 32-element block yields the exact
-// int32 block dots; the per-block scales differ per row and per sequence, so
-// every block gets its own TMEM accumulator, read back and folded in with
-// fmaf(isum, d_w * d_x, acc) (the formula of the dp4a GEMVs).
+//   y[s][r] = sum_b d_w[r][b] * sum_i c[r][b][i] * (d_x[s][b] * q[s][b][i])
+// is a dense contraction.  The weight codes c are exact in fp16 (Q5_0:
+// q - 16 in [-16, 15]; Q8_0: [-127, 127]); each activation value d_x * q is
+// held exactly as two fp16 parts (hi + lo) in an operand image written once
+// per step; every product is exact in fp32.  The weight scale differs per
+// row and per block, so every block of a stage gets its own TMEM accumulator
+// (four MMAs: two 16-wide K steps x two parts), read back and folded in with
+// acc = fmaf(block sum, d_w, acc) in block order.
 //
 // CTA = 128 weight rows (MMA M) x NT sequences (MMA N, up to 64: every
 // weight row is converted once per 64 sequences) x a range of the K stages
@@ -22,12 +23,12 @@
 //                        fp16 A tile (K-major, no swizzle, 8-row x 16-byte
 //                        core matrices) and the weight scales; 3 slots.
 //   MMA warp (1)         TMEM allocation; bulk copies of the activation
-//                        operand (codes + scales, written once per step in
+//                        operand (hi and lo parts, written once per step in
 //                        the MMA layout by the kernel that produced the
-//                        activations; 4 slots); per stage 8 MMAs into 4 TMEM
+//                        activations; 3 slots); per stage 16 MMAs into 4 TMEM
 //                        accumulators of NT columns (2 slots), one commit.
 //   read-back (8 warps)  warp w: TMEM lanes 32 (w % 4).. (its rows), half the
-//                        columns; acc += dot * (d_w * d_x), two lanes per
+//                        columns; acc += block sum * d_w, two lanes per
 //                        packed fp32 instruction (each rounded as the scalar
 //                        fmaf); then frees the stage's slots.
 //
@@ -50,8 +51,8 @@ constexpr int TW_CONS = 8;                     // read-back warps 0..7
 constexpr int TW_PROD = 8;                     // conversion warps 8..15
 constexpr int TW_MMA_WARP = TW_CONS + TW_PROD;  // warp 16: TMEM, bulk copies, MMAs
 constexpr int TW_THREADS = 32 * (TW_MMA_WARP + 1);
-// rings: A tiles + weight scales, activation stages, TMEM slots
-constexpr int TW_NA = 3, TW_NB = 4, TW_NTM = 2;
+// rings: stage slots (A tile + weight scales + activation stage), TMEM slots
+constexpr int TW_NA = 3, TW_NTM = 2;
 constexpr size_t TP_A_BYTES = static_cast<size_t>(TP_M) * TP_BPS * 32 * 2;  // 32 KB
 constexpr size_t TP_DW_BYTES = static_cast<size_t>(TP_DWS) * TP_BPS * 4;
 
@@ -63,12 +64,12 @@ __host__ __device__ inline TpSmem tp_smem() {
     size_t o = 0;
     L.a = o;  // TW_NA A tiles (later the sums [TP_M][NT + 1])
     o += TW_NA * TP_A_BYTES;
-    L.b = o;  // TW_NB activation stages (codes + scales)
-    o += static_cast<size_t>(TW_NB) * IMG_STAGE_BYTES;
+    L.b = o;  // TW_NA activation stages (hi and lo parts)
+    o += static_cast<size_t>(TW_NA) * IMG_STAGE_BYTES;
     L.dw = o;  // TW_NA x dw[j][row]
     o += TW_NA * TP_DW_BYTES;
     L.bar = o;
-    o += static_cast<size_t>(2 * TW_NA + 2 * TW_NB + 2 * TW_NTM) * 8;
+    o += static_cast<size_t>(2 * TW_NA + 2 * TW_NTM) * 8;
     L.tmem = o;
     o += 16;
     L.ticket = o;
@@ -222,8 +223,7 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
     const uint8_t *img = OPROJ ? a.aimg : a.ximg;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
     uint64_t *a_full = bars, *a_empty = bars + TW_NA;
-    uint64_t *b_full = bars + 2 * TW_NA, *b_empty = b_full + TW_NB;
-    uint64_t *tm_full = b_empty + TW_NB, *tm_empty = tm_full + TW_NTM;
+    uint64_t *tm_full = bars + 2 * TW_NA, *tm_empty = tm_full + TW_NTM;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.tmem);
     auto a_tile = [&](int i) { return smem + L.a + static_cast<size_t>(i) * TP_A_BYTES; };
     auto dw_of = [&](int i) { return reinterpret_cast<float *>(smem + L.dw + static_cast<size_t>(i) * TP_DW_BYTES); };
@@ -234,10 +234,6 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
         for (int i = 0; i < TW_NA; ++i) {
             mbar_init(a_full + i, TW_PROD);
             mbar_init(a_empty + i, TW_CONS);
-        }
-        for (int i = 0; i < TW_NB; ++i) {
-            mbar_init(b_full + i, 1);
-            mbar_init(b_empty + i, TW_CONS);
         }
         for (int i = 0; i < TW_NTM; ++i) {
             mbar_init(tm_full + i, 1);
@@ -282,24 +278,54 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
             if (hi > lo) prefetch_l2(W + lo, static_cast<uint32_t>(hi - lo));
         }
         const __half2 wbias = __half2half2(__float2half(wq8 ? 1152.0f : 1040.0f));
-        uint32_t rc[TP_PAIR_WORDS], rn[TP_PAIR_WORDS];
-        load_pair(wrow + static_cast<size_t>(k0) * (TP_BPS / 2) * pb, wq8, rc);
-        for (int t = 0; t < T; ++t) {
-            if (t + 1 < T) load_pair(wrow + static_cast<size_t>(k0 + t + 1) * (TP_BPS / 2) * pb, wq8, rn);
-            const int i = t % TW_NA, n = t / TW_NA;
-            if (n >= 1 && !mbar_wait(a_empty + i, (n - 1) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+        auto decode = [&](int i, const uint32_t (&raw)[TP_PAIR_WORDS]) {
             uint32_t c0[8], c1[8];
             float d0, d1;
             if (wq8)
-                decode_q8_pair(rc, c0, c1, d0, d1);
+                decode_q8_pair(raw, c0, c1, d0, d1);
             else
-                decode_q5_pair(rc, c0, c1, d0, d1);
+                decode_q5_pair(raw, c0, c1, d0, d1);
             uint8_t *tile_a = a_tile(i);
             put_block(tile_a, cr, 2 * cp, c0, wbias);
             put_block(tile_a, cr, 2 * cp + 1, c1, wbias);
             float *dw = dw_of(i);
             dw[(2 * cp) * TP_DWS + cr] = d0;
             dw[(2 * cp + 1) * TP_DWS + cr] = d1;
+        };
+        // activation stage t (hi and lo parts of NT rows) into slot t % TW_NA:
+        // 16-byte async copies, one commit group per stage
+        constexpr int BCH = 2 * NT * (IMG_RG_BYTES / 8) / 16;  // 16-byte chunks
+        auto copy_b = [&](int t) {
+            const uint8_t *src = img + img_stage(G, k0 + t, g);
+            uint8_t *dst = b_stage(t % TW_NA);
+#pragma unroll
+            for (int u = 0; u < BCH / (32 * TW_PROD); ++u) {
+                const int c = pt + 32 * TW_PROD * u;
+                const int part = c / (BCH / 2), off = (c % (BCH / 2)) * 16;
+                cp_async16(dst + part * IMG_CODE_BYTES + off, src + part * IMG_CODE_BYTES + off);
+            }
+            cp_async_commit();
+        };
+        uint32_t rc[TP_PAIR_WORDS], rn[TP_PAIR_WORDS];
+        load_pair(wrow + static_cast<size_t>(k0) * (TP_BPS / 2) * pb, wq8, rc);
+        decode(0, rc);  // the first stage's weights before the wait on the preceding grid
+        pdl_wait();     // the activation image is ready
+        copy_b(0);
+        for (int t = 0; t < T; ++t) {
+            const int i = t % TW_NA;
+            if (t + 1 < T) {
+                load_pair(wrow + static_cast<size_t>(k0 + t + 1) * (TP_BPS / 2) * pb, wq8, rn);
+                // slot (t + 1) % TW_NA is free once stage t + 1 - TW_NA is read back
+                const int n1 = (t + 1) / TW_NA;
+                if (n1 >= 1 && !mbar_wait(a_empty + (t + 1) % TW_NA, (n1 - 1) & 1)) flag_error(a.status, FLAG_TIMEOUT);
+                copy_b(t + 1);
+            }
+            if (t > 0) decode(i, rc);
+            // this stage's activation copies have landed (the next stage's may be in flight)
+            if (t + 1 < T)
+                cp_async_wait<1>();
+            else
+                cp_async_wait<0>();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(a_full + i);
@@ -307,95 +333,86 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
             for (int w = 0; w < TP_PAIR_WORDS; ++w) rc[w] = rn[w];
         }
     } else if (warp == TW_MMA_WARP) {
-        // ---- MMA warp: activation stages (bulk copies, TW_NB in flight)
-        // and the MMAs of each stage into its TMEM slot
+        // ---- MMA warp: the MMAs of each stage into its TMEM slot
         if (lane == 0) {
-            pdl_wait();  // the activation image is ready
-            auto copy_b = [&](int t) {
-                const int i = t % TW_NB;
-                uint8_t *dst = b_stage(i);
-                const uint8_t *src = img + img_stage(G, k0 + t, g);
-                mbar_arrive_expect_tx(b_full + i, NT * (IMG_RG_BYTES / 8) + IMG_BPS * IMG_SEQ * 4);
-                bulk_g2s(dst, src, NT * (IMG_RG_BYTES / 8), b_full + i);
-                bulk_g2s(dst + IMG_CODE_BYTES, src + IMG_CODE_BYTES, IMG_BPS * IMG_SEQ * 4, b_full + i);
-            };
-            for (int t = 0; t < T && t < TW_NB; ++t) copy_b(t);
             const uint32_t idesc =
                 (1u << 4) | (static_cast<uint32_t>(NT >> 3) << 17) | (static_cast<uint32_t>(TP_M >> 4) << 24);
             for (int t = 0; t < T; ++t) {
-                const int ia = t % TW_NA, ib = t % TW_NB, im = t % TW_NTM;
+                const int ia = t % TW_NA, ib = ia, im = t % TW_NTM;
                 bool ok = mbar_wait(a_full + ia, (t / TW_NA) & 1);
-                ok = mbar_wait(b_full + ib, (t / TW_NB) & 1) && ok;
                 if (t >= TW_NTM) ok = mbar_wait(tm_empty + im, (t / TW_NTM - 1) & 1) && ok;
                 if (!ok) flag_error(a.status, FLAG_TIMEOUT);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t abase = sptr(a_tile(ia)), bbase = sptr(b_stage(ib));
+                // descriptors of the stage's tiles; a K step or the lo part is
+                // an offset of the 16-byte-unit start address (shared memory
+                // addresses stay below 256 KB: no carry out of its 14 bits)
+                const uint64_t adesc = tp_desc(sptr(a_tile(ia))), bdesc = tp_desc(sptr(b_stage(ib)));
                 const uint32_t dcol = taddr + im * TP_BPS * NT;
+                // block j: codes x (hi + lo) over its two 16-wide K steps
 #pragma unroll
                 for (int j = 0; j < TP_BPS; ++j)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t ad = tp_desc(abase + (4 * j + 2 * h) * 128);
-                        const uint64_t bd = tp_desc(bbase + (4 * j + 2 * h) * 128);
+                    for (int m = 0; m < 4; ++m) {
+                        const int h = m >> 1, part = m & 1;
+                        const uint64_t ad = adesc + static_cast<uint64_t>((4 * j + 2 * h) * 8);
+                        const uint64_t bd = bdesc + static_cast<uint64_t>(part * (IMG_CODE_BYTES / 16) + (4 * j + 2 * h) * 8);
                         asm volatile(
                             "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dcol + j * NT),
-                            "l"(ad), "l"(bd), "r"(idesc), "r"(h)
+                            "l"(ad), "l"(bd), "r"(idesc), "r"(m)
                             : "memory");
                     }
                 asm volatile(
                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sptr(tm_full + im))
                     : "memory");
-                // stage t - 1 read back: its activation slot takes stage t + TW_NB - 1
-                if (t >= 1 && t + TW_NB - 1 < T) {
-                    if (!mbar_wait(b_empty + (t - 1) % TW_NB, ((t - 1) / TW_NB) & 1))
-                        flag_error(a.status, FLAG_TIMEOUT);
-                    copy_b(t + TW_NB - 1);
-                }
             }
         }
         __syncwarp();
     } else {
         // ---- consumers: fold each block's exact dots in with its two scales
         for (int t = 0; t < T; ++t) {
-            const int ia = t % TW_NA, ib = t % TW_NB, im = t % TW_NTM;
-            // the stage's MMAs are done; the scales written by the producers
-            // and by the bulk copy are acquired from their own barriers (whose
-            // next phases need this stage's release, so they are current)
+            const int ia = t % TW_NA, im = t % TW_NTM;
+            // the stage's MMAs are done; the weight scales written by the
+            // producers are acquired from their own barrier (whose next phase
+            // needs this stage's release, so it is current)
             bool ok = mbar_wait(tm_full + im, (t / TW_NTM) & 1);
             ok = mbar_wait(a_full + ia, (t / TW_NA) & 1) && ok;
-            ok = mbar_wait(b_full + ib, (t / TW_NB) & 1) && ok;
             if (!ok) flag_error(a.status, FLAG_TIMEOUT);
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const float *dw = dw_of(ia) + r;
-            const float *dx = reinterpret_cast<const float *>(b_stage(ib) + IMG_CODE_BYTES);
             const uint32_t base = taddr + (static_cast<uint32_t>((warp & 3) * 32) << 16) + im * TP_BPS * NT + c0;
-            constexpr int CH = CW < 16 ? CW : 16;  // columns per TMEM load
+            // 8 columns per TMEM load, software-pipelined:
+            // chunk c + 1 loads while chunk c is folded in
+            constexpr int CH = 8;
+            constexpr int NCH = TP_BPS * (CW / CH);  // chunks per stage
+            auto ld_chunk = [&](int c, uint32_t *v) {
+                const uint32_t at = base + (c / (CW / CH)) * NT + (c % (CW / CH)) * CH;
+                if constexpr (CH == 16)
+                    tmem_ld16(at, v);
+                else
+                    tmem_ld8(at, v);
+            };
+            uint32_t va[CH], vb[CH];
+            ld_chunk(0, va);
 #pragma unroll
-            for (int j = 0; j < TP_BPS; ++j) {
+            for (int c = 0; c < NCH; ++c) {
+                uint32_t *cur = (c & 1) ? vb : va;
+                uint32_t *nxt = (c & 1) ? va : vb;
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c + 1 < NCH) ld_chunk(c + 1, nxt);
+                const int j = c / (CW / CH), h = c % (CW / CH);
                 const float dwv = dw[j * TP_DWS];
                 const uint64_t dw2 = f2_pack(__float_as_uint(dwv), __float_as_uint(dwv));
-                const uint64_t *dx2 = reinterpret_cast<const uint64_t *>(dx + j * IMG_SEQ + c0);
 #pragma unroll
-                for (int c = 0; c < CW / CH; ++c) {
-                    uint32_t v[CH];
-                    if constexpr (CH == 16)
-                        tmem_ld16(base + j * NT + CH * c, v);
-                    else
-                        tmem_ld8(base + j * NT + CH * c, v);
-                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-                    for (int p = 0; p < CH / 2; ++p)
-                        acc[c * CH / 2 + p] = f2_fma(f2_pack(v[2 * p], v[2 * p + 1]),
-                                                     f2_mul(dw2, dx2[c * CH / 2 + p]), acc[c * CH / 2 + p]);
-                }
+                for (int p = 0; p < CH / 2; ++p)
+                    acc[h * CH / 2 + p] = f2_fma(f2_pack(cur[2 * p], cur[2 * p + 1]), dw2, acc[h * CH / 2 + p]);
             }
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(tm_empty + im);
                 mbar_arrive(a_empty + ia);
-                mbar_arrive(b_empty + ib);
             }
         }
     }

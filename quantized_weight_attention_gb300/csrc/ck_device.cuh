@@ -90,6 +90,17 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (both addresses
+// 16-byte aligned), its commit groups and the wait for all but N groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sptr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Hint: bring [p, p+bytes) into L2 (16-byte aligned address and size).
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -158,19 +169,21 @@ __host__ __device__ constexpr size_t xpack_bytes(int nb) {
 
 // ---------------------------------------------------------------------------
 // Operand image of a batch of Q8_0 activation rows for the tensor-core
-// projections.  Rows (sequences) go in groups of IMG_SEQ, blocks in stages of
-// IMG_BPS (128 codes).  Stage k of group g holds 16 KB of codes as fp16 in
-// the MMA operand layout (core matrices of 8 rows x 8 codes = 128 bytes, 16
-// of them along K per 8-row group, 8-row groups IMG_RG_BYTES apart), then the
-// IMG_BPS x IMG_SEQ block scales (fp32, [block][row]).  A CTA takes a stage's
-// rows with one bulk copy of the codes and one of the scales.
+// projections.  Each value d * q (d the block's fp16 scale, q its code: at
+// most 18 significant bits, exact in fp32) is held exactly as the sum of two
+// fp16 values, hi = fp16(d * q) and lo = d * q - hi (at most 7 significant
+// bits); |d * q| must stay within the fp16 range.  Rows (sequences) go in
+// groups of IMG_SEQ, blocks in stages of IMG_BPS (128 values).  Stage k of
+// group g holds 16 KB of the hi parts in the MMA operand layout (core
+// matrices of 8 rows x 8 values = 128 bytes, 16 of them along K per 8-row
+// group, 8-row groups IMG_RG_BYTES apart), then 16 KB of the lo parts.
 // ---------------------------------------------------------------------------
 constexpr int IMG_SEQ = 64;
 constexpr int IMG_BPS = 4;
-constexpr int IMG_KG = IMG_BPS * 4;                                      // 8-code groups along K
-constexpr int IMG_RG_BYTES = IMG_KG * 128;                               // one 8-row group
-constexpr int IMG_CODE_BYTES = IMG_SEQ / 8 * IMG_RG_BYTES;               // 16 KB
-constexpr int IMG_STAGE_BYTES = IMG_CODE_BYTES + IMG_BPS * IMG_SEQ * 4;  // + 1 KB of scales
+constexpr int IMG_KG = IMG_BPS * 4;                         // 8-value groups along K
+constexpr int IMG_RG_BYTES = IMG_KG * 128;                  // one 8-row group
+constexpr int IMG_CODE_BYTES = IMG_SEQ / 8 * IMG_RG_BYTES;  // 16 KB: one part
+constexpr int IMG_STAGE_BYTES = 2 * IMG_CODE_BYTES;         // hi, then lo
 __host__ __device__ constexpr int img_groups(int B) { return (B + IMG_SEQ - 1) / IMG_SEQ; }
 __host__ __device__ constexpr size_t img_bytes(int nb, int B) {
     return static_cast<size_t>(nb / IMG_BPS) * img_groups(B) * IMG_STAGE_BYTES;
@@ -178,31 +191,18 @@ __host__ __device__ constexpr size_t img_bytes(int nb, int B) {
 __host__ __device__ constexpr size_t img_stage(int G, int k, int g) {
     return (static_cast<size_t>(k) * G + g) * IMG_STAGE_BYTES;
 }
-// The 16 bytes holding codes 8e .. 8e + 7 of block b of row s.
+// The 16 bytes holding hi parts 8e .. 8e + 7 of block b of row s (the lo
+// parts are IMG_CODE_BYTES further).
 __host__ __device__ constexpr size_t img_code_off(int G, int s, int b, int e) {
     return img_stage(G, b / IMG_BPS, s / IMG_SEQ) + static_cast<size_t>(((s % IMG_SEQ) >> 3) * IMG_RG_BYTES) +
            static_cast<size_t>(((b % IMG_BPS) * 4 + e) * 128 + (s & 7) * 16);
 }
-__host__ __device__ constexpr size_t img_d_off(int G, int s, int b) {
-    return img_stage(G, b / IMG_BPS, s / IMG_SEQ) + IMG_CODE_BYTES +
-           static_cast<size_t>((b % IMG_BPS) * IMG_SEQ + s % IMG_SEQ) * 4;
-}
-// Eight signed Q8_0 codes (two words, element order) as eight fp16 values,
-// exactly: byte u = q + 128 becomes the fp16 1024 + u, minus 1152.
-__device__ __forceinline__ uint4 q8_codes_to_half8(uint32_t w0, uint32_t w1) {
-    const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152
-    uint32_t h[4];
-    const uint32_t c[2] = {w0 ^ 0x80808080u, w1 ^ 0x80808080u};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const uint32_t lo = __byte_perm(c[i], 0x64646464u, 0x5140);
-        const uint32_t hi = __byte_perm(c[i], 0x64646464u, 0x7362);
-        const __half2 a = __hsub2(*reinterpret_cast<const __half2 *>(&lo), bias);
-        const __half2 b = __hsub2(*reinterpret_cast<const __half2 *>(&hi), bias);
-        h[2 * i] = *reinterpret_cast<const uint32_t *>(&a);
-        h[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&b);
-    }
-    return make_uint4(h[0], h[1], h[2], h[3]);
+// The exact fp16 pair of d * q (false when it leaves the fp16 range).
+__device__ __forceinline__ bool img_split(float d, int q, __half &hi, __half &lo) {
+    const float v = d * static_cast<float>(q);  // exact
+    hi = __float2half_rn(v);
+    lo = __float2half_rn(v - __half2float(hi));  // exact residual
+    return fabsf(v) <= 65504.0f;
 }
 
 struct XRow {
