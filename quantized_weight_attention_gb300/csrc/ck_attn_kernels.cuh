@@ -444,29 +444,34 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
             }
         }
     }
-    consumers_sync();
-    for (int idx = ct; idx < G * HD; idx += 32 * AT_CONSUMERS) {
-        const int j = idx / HD;
+    // each warp's weight exp2(m_w - M) per head once (the same values, in the
+    // same order, as a per-element evaluation), the record's m and l
+    float *scw = reinterpret_cast<float *>(smem + L.off_alpha);  // [NC][GMAX]
+    if (ct < G) {
+        const int j = ct;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < AT_CONSUMERS; ++w) M = fmaxf(M, mlw[w * GMAX + j]);
-        float t = 0.0f;
+        float Ls = 0.0f;
 #pragma unroll
         for (int w = 0; w < AT_CONSUMERS; ++w) {
             const float mw = mlw[w * GMAX + j];
-            if (mw != -INFINITY) t = fmaf(exp2f(mw - M), accw[(w * G + j) * HD + (idx - j * HD)], t);
+            const float sc = (mw != -INFINITY) ? exp2f(mw - M) : 0.0f;
+            scw[w * GMAX + j] = sc;
+            if (mw != -INFINITY) Ls = fmaf(sc, mlw[(AT_CONSUMERS + w) * GMAX + j], Ls);
+        }
+        rec[j] = M;
+        rec[G + j] = Ls;
+    }
+    consumers_sync();
+    for (int idx = ct; idx < G * HD; idx += 32 * AT_CONSUMERS) {
+        const int j = idx / HD;
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < AT_CONSUMERS; ++w) {
+            if (mlw[w * GMAX + j] != -INFINITY) t = fmaf(scw[w * GMAX + j], accw[(w * G + j) * HD + (idx - j * HD)], t);
         }
         rec[2 * G + idx] = t;
-        if (idx - j * HD == 0) {
-            float Ls = 0.0f;
-#pragma unroll
-            for (int w = 0; w < AT_CONSUMERS; ++w) {
-                const float mw = mlw[w * GMAX + j];
-                if (mw != -INFINITY) Ls = fmaf(exp2f(mw - M), mlw[(AT_CONSUMERS + w) * GMAX + j], Ls);
-            }
-            rec[j] = M;
-            rec[G + j] = Ls;
-        }
     }
 }
 

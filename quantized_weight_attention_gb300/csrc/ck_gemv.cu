@@ -459,6 +459,18 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
     }
     const bool q8 = T.kind == 2;
     if (threadIdx.x == 0) stage_qkv_rows(a, nw, wst, bar, rb5, rb8);  // the weights do not depend on earlier grids
+    // the epilogue's constant operands (biases, RoPE table entries) before the wait
+    const int half = a.hd >> 1;
+    float ea = 0.0f, eb = 0.0f, ec = 1.0f, es = 0.0f;
+    if (lane == 0 && T.kind != 3) {
+        const float *bias = T.kind == 0 ? a.bq : T.kind == 1 ? a.bk : a.bv;
+        ea = bias ? bias[T.ra] : 0.0f;
+        eb = bias ? bias[T.rb] : 0.0f;
+        if (T.kind != 2) {
+            ec = a.rope_cos[static_cast<size_t>(pos) * half + T.i];
+            es = a.rope_sin[static_cast<size_t>(pos) * half + T.i];
+        }
+    }
     pdl_trigger();
     if (a.fused_norm) {
         float gv[NORM_XPW];  // gamma does not depend on the preceding grid
@@ -481,8 +493,8 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
     const float sb = __shfl_sync(0xffffffffu, acc, 16);
     if (lane != 0) return;
     if (T.kind == 2) {
-        const float va = acc + (a.bv ? a.bv[T.ra] : 0.0f);
-        const float vb = sb + (a.bv ? a.bv[T.rb] : 0.0f);
+        const float va = acc + ea;
+        const float vb = sb + eb;
         int h = T.ra / a.hd;
         a.v_cache[(static_cast<size_t>(h) * a.C + pos) * a.hd + (T.ra - h * a.hd)] = va;
         h = T.rb / a.hd;
@@ -490,14 +502,10 @@ __global__ void __launch_bounds__(512, 1) k_qkv_w(const QkvArgs a) {
         return;
     }
     // bias, then rotate-half RoPE of the pair (i, i + hd/2) at row `pos`
-    const int half = a.hd >> 1;
-    const float *bias = T.kind == 0 ? a.bq : a.bk;
-    const float A = acc + (bias ? bias[T.ra] : 0.0f);
-    const float B = sb + (bias ? bias[T.rb] : 0.0f);
-    const float c = a.rope_cos[static_cast<size_t>(pos) * half + T.i];
-    const float s = a.rope_sin[static_cast<size_t>(pos) * half + T.i];
-    const float A2 = __fsub_rn(__fmul_rn(A, c), __fmul_rn(B, s));
-    const float B2 = __fadd_rn(__fmul_rn(A, s), __fmul_rn(B, c));
+    const float A = acc + ea;
+    const float B = sb + eb;
+    const float A2 = __fsub_rn(__fmul_rn(A, ec), __fmul_rn(B, es));
+    const float B2 = __fadd_rn(__fmul_rn(A, es), __fmul_rn(B, ec));
     if (T.kind == 0) {
         a.q_out[T.ra] = A2;
         a.q_out[T.rb] = B2;
@@ -534,8 +542,19 @@ __global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
         mbar_arrive_expect_tx(bar, bytes);
         bulk_g2s_run(smem + L.off_w, a.wo + static_cast<size_t>(rw0) * rb, bytes, bar);
     }
+    // the bias (a constant input) before the wait; the residual may be the
+    // previous layer's output, so it is loaded after the wait, ahead of the dot
+    float ba = 0.0f, bb = 0.0f, ra = 0.0f, rbv = 0.0f;
+    if (lane == 0 && valid && a.bo) {
+        ba = a.bo[r0];
+        bb = a.bo[r0 + 1];
+    }
     pdl_trigger();
     pdl_wait();  // the attention output is ready
+    if (lane == 0 && valid) {
+        ra = a.residual[r0];
+        rbv = a.residual[r0 + 1];
+    }
     if (a.apack)
         xrow_from_pack(a.apack, nb, x);
     else
@@ -545,8 +564,8 @@ __global__ void __launch_bounds__(512, 1) k_oproj_w(const OprojArgs a) {
     const float acc = warp_row_dot<false>(slot + (lane >> 4) * rb, nseg, lane & 15, x);
     const float sb = __shfl_sync(0xffffffffu, acc, 16);
     if (lane == 0) {
-        a.out[r0] = (acc + (a.bo ? a.bo[r0] : 0.0f)) + a.residual[r0];
-        a.out[r0 + 1] = (sb + (a.bo ? a.bo[r0 + 1] : 0.0f)) + a.residual[r0 + 1];
+        a.out[r0] = (acc + ba) + ra;
+        a.out[r0 + 1] = (sb + bb) + rbv;
     }
 }
 
