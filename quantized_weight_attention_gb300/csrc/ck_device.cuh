@@ -442,9 +442,13 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
 // ---------------------------------------------------------------------------
 // rstd = 1/sqrt(mean + eps) from every thread's (sum, compensation) pair of
 // x^2 terms: the pairs are combined with two-sums (warp, then CTA), so the
-// total equals the double-precision sum to ~2^-46 relative; rstd is then
-// formed in double and rounded once to fp32.  `red` holds 2*warps + 1
-// floats.  Every thread of the CTA gets rstd.
+// total equals the double-precision sum to ~2^-46 relative.  m = sum/D + eps
+// is carried as an fp32 pair (hi + lo); rstd is the hardware reciprocal
+// square root of hi refined by one Newton-Raphson step for 1/sqrt(m),
+// y + y (1 - m y^2) / 2, whose residual is formed with FMAs over the pair
+// terms (error ~2^-44), then rounded once to fp32.  (fp64 arithmetic, which
+// this replaces, runs at a small fraction of the fp32 rate on this GPU.)
+// `red` holds 2*warps + 1 floats.  Every thread of the CTA gets rstd.
 __device__ inline float rstd_from_pairs(float s, float c, int D, float eps, float *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
@@ -474,8 +478,16 @@ __device__ inline float rstd_from_pairs(float s, float c, int D, float eps, floa
             c = __fadd_rn(__fadd_rn(c, c2), err);
         }
         if (lane == 0) {
-            const double ss = static_cast<double>(s) + static_cast<double>(c);
-            red[2 * nw] = static_cast<float>(1.0 / sqrt(ss / static_cast<double>(D) + static_cast<double>(eps)));
+            const float Df = static_cast<float>(D);  // exact: D < 2^24
+            const float qh = __fdiv_rn(s, Df);
+            const float ql = __fdiv_rn(__fadd_rn(fmaf(-qh, Df, s), c), Df);  // (s - qh D) exactly, plus c
+            float mh, e;
+            two_sum(qh, eps, mh, e);
+            const float ml = __fadd_rn(ql, e);
+            const float y = rsqrtf(mh);
+            const float p = __fmul_rn(y, y), pl = fmaf(y, y, -p);        // y^2 = p + pl exactly
+            const float h = fmaf(-mh, pl, fmaf(-ml, p, fmaf(-mh, p, 1.0f)));  // 1 - m y^2
+            red[2 * nw] = fmaf(0.5f * y, h, y);
         }
     }
     __syncthreads();
@@ -514,26 +526,44 @@ __device__ inline void norm_quant_xrow(const float *x, const float (&gv)[NORM_XP
 #pragma unroll
     for (int j = 0; j < NORM_XPW; ++j) sumsq_add(xv[j], s, c);
     const float rstd = rstd_from_pairs(s, c, D, eps, red);
+    // quantize_row_q8_0 of the warp's blocks, all of them at once: amax by
+    // one warp reduction over the bit patterns of |y| (non-negative floats
+    // order as their bits), d = amax / 127, codes round(y / d), code sums
+    float y[NORM_XPW];
+    unsigned am[NORM_XPW];
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        y[j] = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
+        am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(y[j])));
+    }
+    int q[NORM_XPW];
+    float dq[NORM_XPW];
+    uint32_t dbits[NORM_XPW];
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j) {
+        const float d = __fdiv_rn(__uint_as_float(am[j]), 127.0f);
+        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+        const __half dh = __float2half_rn(d);
+        dbits[j] = __half_as_ushort(dh);
+        dq[j] = __half2float(dh);
+        q[j] = static_cast<int>(roundf(__fmul_rn(y[j], id)));
+    }
 #pragma unroll
     for (int j = 0; j < NORM_XPW; ++j) {
         const int b = warp + nw * j;
+        const int sum = __reduce_add_sync(0xffffffffu, q[j]);
         if (b < nb) {  // warp-uniform
-            const float y = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
-            uint32_t dbits;
-            float dq;
-            const int q = q8_code(y, dbits, dq);
-            reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q);
-            const int sum = warp_isum(q);
+            reinterpret_cast<int8_t *>(&xr.q[xq_chunk(b, lane >> 4)])[lane & 15] = static_cast<int8_t>(q[j]);
             if (lane == 0) {
-                xr.d[b] = dq;
+                xr.d[b] = dq[j];
                 xr.sum[b] = sum;
             }
             if (tap) {
                 uint8_t *o = tap + static_cast<size_t>(b) * Q8B;
-                o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+                o[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q[j]));
                 if (lane == 0) {
-                    o[0] = static_cast<uint8_t>(dbits & 0xFF);
-                    o[1] = static_cast<uint8_t>(dbits >> 8);
+                    o[0] = static_cast<uint8_t>(dbits[j] & 0xFF);
+                    o[1] = static_cast<uint8_t>(dbits[j] >> 8);
                 }
             }
         }
