@@ -536,16 +536,23 @@ __device__ inline void norm_quant_xrow(const float *x, const float (&gv)[NORM_XP
         y[j] = __fmul_rn(__fmul_rn(xv[j], rstd), gv[j]);
         am[j] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(y[j])));
     }
+    // d = amax / 127, 1 / d and the fp16 scale of block j on lane j, then
+    // broadcast (the same values on every lane, computed once per block)
+    float myam = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NORM_XPW; ++j)
+        if (lane == j) myam = __uint_as_float(am[j]);
+    const float dl = __fdiv_rn(myam, 127.0f);
+    const float idl = (dl != 0.0f) ? __frcp_rn(dl) : 0.0f;
+    const uint32_t dbl = __half_as_ushort(__float2half_rn(dl));
     int q[NORM_XPW];
     float dq[NORM_XPW];
     uint32_t dbits[NORM_XPW];
 #pragma unroll
     for (int j = 0; j < NORM_XPW; ++j) {
-        const float d = __fdiv_rn(__uint_as_float(am[j]), 127.0f);
-        const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
-        const __half dh = __float2half_rn(d);
-        dbits[j] = __half_as_ushort(dh);
-        dq[j] = __half2float(dh);
+        const float id = __shfl_sync(0xffffffffu, idl, j);
+        dbits[j] = __shfl_sync(0xffffffffu, dbl, j);
+        dq[j] = __half2float(__ushort_as_half(static_cast<unsigned short>(dbits[j])));
         q[j] = static_cast<int>(roundf(__fmul_rn(y[j], id)));
     }
 #pragma unroll
