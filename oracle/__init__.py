@@ -67,6 +67,19 @@ def lib():
             L.ref_block_dot_q8_0_q8_0.argtypes = [P, P]
             L.ref_block_dots.argtypes = [P, P, P, i, i, i]
             L.ref_gemv.argtypes = [P, P, P, P, i, i, i]
+            L.ref_bf16_to_f32.restype = f
+            L.ref_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            L.ref_f32_to_bf16.restype = ctypes.c_uint16
+            L.ref_f32_to_bf16.argtypes = [f]
+            L.ref_e4m3_to_f32.restype = f
+            L.ref_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            L.ref_f32_to_e4m3.restype = ctypes.c_uint8
+            L.ref_f32_to_e4m3.argtypes = [f]
+            L.ref_f32_to_bf16_n.argtypes = [P, P, ctypes.c_long]
+            L.ref_f32_to_e4m3_n.argtypes = [P, f, P, ctypes.c_long]
+            L.ref_e4m3_to_f32_n.argtypes = [P, P, ctypes.c_long]
+            L.ref_attention_kvq.argtypes = [P, P, P, P, i, i, i, i, i, i, f, f]
+            L.ref_kv_store_kvq.argtypes = [P, P, P, P, i, i, i, i, i, f, f]
             L.ref_rmsnorm.restype = f
             L.ref_rmsnorm.argtypes = [P, P, P, i, f]
             L.ref_rope.argtypes = [P, P, P, P, i, i, i, i]
@@ -200,6 +213,57 @@ def attention(q, k_cache, v_cache, H: int, KV: int, T: int, capacity: int, hd: i
     out = np.empty(H * hd, np.float32)
     lib().ref_attention(_p(_f32(q)), _p(_f32(k_cache)), _p(_f32(v_cache)), _p(out), H, KV, T, capacity, hd)
     return out
+
+
+# ---- reduced-precision KV caches (bf16; fp8 E4M3 with per-tensor scales) ----
+KV_BF16, KV_FP8 = 1, 2
+
+
+def bf16_from_f32(x) -> np.ndarray:
+    """bfloat16 bit patterns of x (round to nearest, ties to even)."""
+    x = _f32(x)
+    y = np.empty(x.size, np.uint16)
+    lib().ref_f32_to_bf16_n(_p(x), _p(y), x.size)
+    return y.reshape(x.shape)
+
+
+def bf16_to_f32(b) -> np.ndarray:
+    return (np.ascontiguousarray(b, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def e4m3_from_f32(x, scale: float = 1.0) -> np.ndarray:
+    """E4M3 codes of x / scale (round to nearest even, saturated to +-448)."""
+    x = _f32(x)
+    y = np.empty(x.size, np.uint8)
+    lib().ref_f32_to_e4m3_n(_p(x), float(scale), _p(y), x.size)
+    return y.reshape(x.shape)
+
+
+def e4m3_to_f32(c) -> np.ndarray:
+    c = np.ascontiguousarray(c, np.uint8)
+    y = np.empty(c.size, np.float32)
+    lib().ref_e4m3_to_f32_n(_p(c), _p(y), c.size)
+    return y.reshape(c.shape)
+
+
+def attention_kvq(q, k_cache, v_cache, H: int, KV: int, T: int, capacity: int, hd: int, kind: int,
+                  k_scale: float = 1.0, v_scale: float = 1.0) -> np.ndarray:
+    """Decode attention over a bf16 (kind 1) or E4M3 (kind 2) cache [KV, capacity, hd]."""
+    dt = np.uint16 if kind == KV_BF16 else np.uint8
+    kc = np.ascontiguousarray(k_cache, dt)
+    vc = np.ascontiguousarray(v_cache, dt)
+    out = np.empty(H * hd, np.float32)
+    lib().ref_attention_kvq(_p(_f32(q)), _p(kc), _p(vc), _p(out), H, KV, T, capacity, hd, kind, float(k_scale),
+                            float(v_scale))
+    return out
+
+
+def kv_store_kvq(k_cache, v_cache, k, v, pos: int, KV: int, capacity: int, hd: int, kind: int,
+                 k_scale: float = 1.0, v_scale: float = 1.0):
+    """STEP 6 into a reduced cache, in place."""
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    lib().ref_kv_store_kvq(_p(k_cache), _p(v_cache), _p(_f32(k)), _p(_f32(v)), pos, KV, capacity, hd, kind,
+                           float(k_scale), float(v_scale))
 
 
 def decode_layer(x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos, rope_sin,

@@ -347,6 +347,161 @@ void ref_attention(const float *q, const float *k_cache, const float *v_cache, f
 }
 
 /* ------------------------------------------------------------------------
+ * Reduced-precision KV caches (page "paged decode attention" launchers
+ * paged_decode_attn_bf16 / paged_decode_attn_fp8: bf16 and fp8 caches, the
+ * fp8 one with per-tensor k_scale and v_scale; the pages print only the
+ * launchers, so the element formats are taken from their definitions):
+ *
+ * bfloat16: the upper 16 bits of a binary32 (1 sign, 8 exponent, 7 fraction
+ *   bits).  From binary32: round to nearest, ties to even (a NaN stays NaN).
+ * E4M3 ("FN" 8-bit float): 1 sign, 4 exponent bits with bias 7, 3 fraction
+ *   bits; exponent field 0 holds subnormals frac * 2^-9; S.1111.111 is NaN;
+ *   no infinity; the largest finite magnitude is 1.75 * 2^8 = 448.  From
+ *   binary32: round to nearest, ties to even, magnitudes beyond 448
+ *   saturate to 448, NaN gives NaN.
+ * The cache value is the bf16 number, or code * k_scale (keys) and
+ * code * v_scale (values) for E4M3.  A store quantizes x / scale (the IEEE
+ * binary32 quotient).
+ * ---------------------------------------------------------------------- */
+float ref_bf16_to_f32(uint16_t b)
+{
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+uint16_t ref_f32_to_bf16(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, sizeof u);
+    if (isnan(x))
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t t = u >> 16;           /* truncated: the representable value toward zero */
+    const uint32_t r = u & 0xFFFFu; /* the discarded bits */
+    if (r > 0x8000u || (r == 0x8000u && (t & 1u)))
+        t += 1u; /* the next magnitude up (into the exponent, or to infinity) */
+    return (uint16_t)t;
+}
+
+float ref_e4m3_to_f32(uint8_t c)
+{
+    const int e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9); /* (m / 8) * 2^-6 */
+    else
+        v = ldexp(8.0 + m, e - 10); /* (1 + m / 8) * 2^(e - 7) */
+    return (float)((c & 0x80) ? -v : v);
+}
+
+uint8_t ref_f32_to_e4m3(float x)
+{
+    if (isnan(x))
+        return 0x7F;
+    const int sign = signbit(x) ? 0x80 : 0;
+    const double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    /* the nearest of the non-negative finite codes 0x00 .. 0x7E (values
+     * increase with the code); on a tie, the even code */
+    int best = 0;
+    double bd = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs((double)ref_e4m3_to_f32((uint8_t)c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void ref_f32_to_bf16_n(const float *x, uint16_t *y, long n)
+{
+    for (long i = 0; i < n; ++i)
+        y[i] = ref_f32_to_bf16(x[i]);
+}
+
+/* codes of x / scale (binary32 quotients) */
+void ref_f32_to_e4m3_n(const float *x, float scale, uint8_t *y, long n)
+{
+    for (long i = 0; i < n; ++i)
+        y[i] = ref_f32_to_e4m3(x[i] / scale);
+}
+
+void ref_e4m3_to_f32_n(const uint8_t *c, float *y, long n)
+{
+    for (long i = 0; i < n; ++i)
+        y[i] = ref_e4m3_to_f32(c[i]);
+}
+
+/* value of element i of a reduced cache: kind 1 = bf16, 2 = E4M3 * scale */
+static double kvq_value(const void *cache, size_t i, int kind, double scale)
+{
+    if (kind == 1)
+        return (double)ref_bf16_to_f32(((const uint16_t *)cache)[i]);
+    return (double)ref_e4m3_to_f32(((const uint8_t *)cache)[i]) * scale;
+}
+
+/* ref_attention over a bf16 (kind 1) or E4M3 (kind 2) cache: the same
+ * two-pass softmax in double on the caches' values. */
+void ref_attention_kvq(const float *q, const void *k_cache, const void *v_cache, float *out, int H, int KV, int T,
+                       int capacity, int hd, int kind, float k_scale, float v_scale)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *o = (double *)malloc(sizeof(double) * (size_t)hd);
+    const double scale = 1.0 / sqrt((double)hd);
+    for (int h = 0; h < H; ++h) {
+        const int kvh = (int)((long)h * KV / H);
+        const float *qh = q + (size_t)h * hd;
+        const size_t base = (size_t)kvh * capacity * hd;
+        double m = -INFINITY;
+        for (int t = 0; t < T; ++t) {
+            double dot = 0.0;
+            for (int d = 0; d < hd; ++d)
+                dot += (double)qh[d] * kvq_value(k_cache, base + (size_t)t * hd + d, kind, k_scale);
+            s[t] = dot * scale;
+            if (s[t] > m)
+                m = s[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < T; ++t) {
+            s[t] = exp(s[t] - m);
+            l += s[t];
+        }
+        for (int d = 0; d < hd; ++d)
+            o[d] = 0.0;
+        for (int t = 0; t < T; ++t)
+            for (int d = 0; d < hd; ++d)
+                o[d] += s[t] * kvq_value(v_cache, base + (size_t)t * hd + d, kind, v_scale);
+        for (int d = 0; d < hd; ++d)
+            out[(size_t)h * hd + d] = (float)(o[d] / l);
+    }
+    free(s);
+    free(o);
+}
+
+/* STEP 6 into a reduced cache: row pos of every KV head. */
+void ref_kv_store_kvq(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int KV, int capacity,
+                      int hd, int kind, float k_scale, float v_scale)
+{
+    for (int h = 0; h < KV; ++h)
+        for (int d = 0; d < hd; ++d) {
+            const size_t i = ((size_t)h * capacity + pos) * hd + d, j = (size_t)h * hd + d;
+            if (kind == 1) {
+                ((uint16_t *)k_cache)[i] = ref_f32_to_bf16(k[j]);
+                ((uint16_t *)v_cache)[i] = ref_f32_to_bf16(v[j]);
+            } else {
+                ((uint8_t *)k_cache)[i] = ref_f32_to_e4m3(k[j] / k_scale);
+                ((uint8_t *)v_cache)[i] = ref_f32_to_e4m3(v[j] / v_scale);
+            }
+        }
+}
+
+/* ------------------------------------------------------------------------
  * mega_fused_attention_decode_q5_0, in the page's order (STEP 1 .. STEP 8).
  * `dbg_*` are optional (NULL-able) taps of the intermediates:
  *   dbg_xq   [D/32 Q8_0 blocks]   the quantized normed input
