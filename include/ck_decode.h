@@ -139,6 +139,38 @@ int ck_attn_decode_gqa_noalloc(const float *q, const float *k_cache, const float
                                int num_heads, int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim,
                                void *stream);
 
+/* ---- reduced-precision KV caches ---------------------------------------- */
+
+/* The same decode attention over a bf16 or an fp8 cache (page "paged
+ * decode attention" launchers paged_decode_attn_bf16 / paged_decode_attn_fp8:
+ * bf16 and fp8 KV caches, the fp8 one with per-tensor k_scale and v_scale;
+ * here on the head-major layout of ck_attn_decode_gqa, not paged).
+ * k_cache / v_cache: [num_kv_heads, cache_capacity, head_dim] elements of
+ *   - bf16 (ck_attn_decode_gqa_bf16): the value is the bf16 number;
+ *   - fp8 E4M3 (ck_attn_decode_gqa_fp8; 1 sign, 4 exponent bits with bias 7,
+ *     3 mantissa bits, subnormals, largest finite 448, 0x7F / 0xFF are NaN,
+ *     no infinities): the value is code * k_scale (keys), code * v_scale
+ *     (values); k_scale, v_scale finite and > 0 (else CK_EINVAL).
+ * head_dim in {64, 128} (else CK_EINVAL); otherwise the arguments,
+ * requirements, scratch and result of ck_attn_decode_gqa. */
+int ck_attn_decode_gqa_bf16(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                            int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
+                            size_t scratch_bytes, void *stream);
+int ck_attn_decode_gqa_fp8(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                           int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, float k_scale,
+                           float v_scale, void *scratch, size_t scratch_bytes, void *stream);
+
+/* KV-cache store (page: STEP 6) into those caches: k_cache[h][pos][:] and
+ * v_cache[h][pos][:] from the fp32 rows k, v [num_kv_heads * head_dim].
+ * bf16: round to nearest, ties to even.  fp8: code = E4M3(x / scale) with x /
+ * scale the IEEE fp32 quotient, rounded to nearest (ties to even) and
+ * saturated to +-448 (NaN stays NaN).  0 <= pos < cache_capacity (else
+ * CK_ERANGE); fp8 scales finite and > 0 (else CK_EINVAL). */
+int ck_kv_store_bf16(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                     int cache_capacity, int head_dim, void *stream);
+int ck_kv_store_fp8(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                    int cache_capacity, int head_dim, float k_scale, float v_scale, void *stream);
+
 /* ---- the whole layer step ---------------------------------------------- */
 
 /* mega_fused_attention_decode_q5_0 (page: MAIN KERNEL).  One token at

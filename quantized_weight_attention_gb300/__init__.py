@@ -25,7 +25,8 @@ __all__ = [
     "ck_decode_layer_scratch_size", "ck_decode_layer", "ck_decode_layer_devpos", "ck_device_status",
     "ck_block_dots_q5_0_q8_0", "ck_block_dots_q8_0_q8_0", "LIB_PATH", "ck_decode_layer_scratch_offset",
     "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8", "ck_attn_decode_gqa_noalloc",
-    "CK_ATTN_NOALLOC_MAX_BYTES",
+    "CK_ATTN_NOALLOC_MAX_BYTES", "ck_attn_decode_gqa_bf16", "ck_attn_decode_gqa_fp8", "ck_kv_store_bf16",
+    "ck_kv_store_fp8",
 ]
 
 CK_OK, CK_EINVAL, CK_ERANGE, CK_ESCRATCH, CK_EALIGN, CK_ECUDA, CK_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -53,6 +54,10 @@ _SIGS = {
     "ck_kv_store": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "ck_attn_scratch_size": (_SZ, [_I, _I, _I, _I]),
     "ck_attn_decode_gqa": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "ck_attn_decode_gqa_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "ck_attn_decode_gqa_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P, _SZ, _P]),
+    "ck_kv_store_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
+    "ck_kv_store_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
     "ck_attn_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ck_decode_layer_scratch_size": (_SZ, [_I, _I, _I, _I, _I]),
     "ck_decode_layer": (_I, [_P] * 16 + [_I] * 6 + [_F, _P, _SZ, _P]),
@@ -143,6 +148,35 @@ def ck_attn_decode_gqa(q, k_cache, v_cache, out, num_heads: int, num_kv_heads: i
     return lib().ck_attn_decode_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, num_kv_heads,
                                     kv_tokens, cache_capacity, head_dim, _ptr(scratch), scratch_bytes,
                                     _stream(stream))
+
+
+def ck_attn_decode_gqa_bf16(q, k_cache, v_cache, out, num_heads: int, num_kv_heads: int, kv_tokens: int,
+                            cache_capacity: int, head_dim: int, scratch, scratch_bytes: int, stream=None) -> int:
+    """ck_attn_decode_gqa over bf16 caches (head_dim 64 or 128)."""
+    return lib().ck_attn_decode_gqa_bf16(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, num_kv_heads,
+                                         kv_tokens, cache_capacity, head_dim, _ptr(scratch), scratch_bytes,
+                                         _stream(stream))
+
+
+def ck_attn_decode_gqa_fp8(q, k_cache, v_cache, out, num_heads: int, num_kv_heads: int, kv_tokens: int,
+                           cache_capacity: int, head_dim: int, k_scale: float, v_scale: float, scratch,
+                           scratch_bytes: int, stream=None) -> int:
+    """ck_attn_decode_gqa over fp8 E4M3 caches: k = code * k_scale, v = code * v_scale."""
+    return lib().ck_attn_decode_gqa_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), num_heads, num_kv_heads,
+                                        kv_tokens, cache_capacity, head_dim, float(k_scale), float(v_scale),
+                                        _ptr(scratch), scratch_bytes, _stream(stream))
+
+
+def ck_kv_store_bf16(k_cache, v_cache, k, v, pos: int, num_kv_heads: int, cache_capacity: int, head_dim: int,
+                     stream=None) -> int:
+    return lib().ck_kv_store_bf16(_ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v), pos, num_kv_heads,
+                                  cache_capacity, head_dim, _stream(stream))
+
+
+def ck_kv_store_fp8(k_cache, v_cache, k, v, pos: int, num_kv_heads: int, cache_capacity: int, head_dim: int,
+                    k_scale: float, v_scale: float, stream=None) -> int:
+    return lib().ck_kv_store_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v), pos, num_kv_heads, cache_capacity,
+                                 head_dim, float(k_scale), float(v_scale), _stream(stream))
 
 
 CK_ATTN_NOALLOC_MAX_BYTES = 2 * 1024 * 1024

@@ -12,6 +12,7 @@
 // Each kernel after the first is launched with programmatic dependent
 // launch: it starts while its predecessor drains, streams the operands that
 // do not depend on it (weights, cache rows before `pos`), then waits.
+#include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -351,11 +352,65 @@ size_t ck_attn_scratch_size(int num_heads, int num_kv_heads, int max_kv_tokens, 
     return attn_part_bytes(1, num_heads, num_kv_heads, head_dim, S) + 256;
 }
 
+static int attn_call(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                     int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_type, float k_scale,
+                     float v_scale, void *scratch, size_t scratch_bytes, void *stream);
+
 int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int num_heads,
                        int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
                        size_t scratch_bytes, void *stream) {
+    return attn_call(q, k_cache, v_cache, out, num_heads, num_kv_heads, kv_tokens, cache_capacity, head_dim, 0,
+                     1.0f, 1.0f, scratch, scratch_bytes, stream);
+}
+
+static bool scale_ok(float s) { return std::isfinite(s) && s > 0.0f; }
+
+int ck_attn_decode_gqa_bf16(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                            int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
+                            size_t scratch_bytes, void *stream) {
+    return attn_call(q, k_cache, v_cache, out, num_heads, num_kv_heads, kv_tokens, cache_capacity, head_dim,
+                     KV_BF16, 1.0f, 1.0f, scratch, scratch_bytes, stream);
+}
+
+int ck_attn_decode_gqa_fp8(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                           int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, float k_scale,
+                           float v_scale, void *scratch, size_t scratch_bytes, void *stream) {
+    if (!scale_ok(k_scale) || !scale_ok(v_scale)) return CK_EINVAL;
+    return attn_call(q, k_cache, v_cache, out, num_heads, num_kv_heads, kv_tokens, cache_capacity, head_dim, KV_FP8,
+                     k_scale, v_scale, scratch, scratch_bytes, stream);
+}
+
+static int kv_store_q(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                      int cache_capacity, int head_dim, int kv_type, float k_scale, float v_scale, void *stream) {
+    int rc = check_ptrs({k_cache, v_cache, k, v}, {});
+    if (rc) return rc;
+    if (num_kv_heads <= 0 || head_dim <= 0 || cache_capacity <= 0) return CK_EINVAL;
+    if (pos < 0 || pos >= cache_capacity) return CK_ERANGE;
+    return launch_kv_store_q(k_cache, v_cache, k, v, pos, num_kv_heads, cache_capacity, head_dim, kv_type, k_scale,
+                             v_scale, as_stream(stream))
+               ? CK_ECUDA
+               : CK_OK;
+}
+
+int ck_kv_store_bf16(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                     int cache_capacity, int head_dim, void *stream) {
+    return kv_store_q(k_cache, v_cache, k, v, pos, num_kv_heads, cache_capacity, head_dim, KV_BF16, 1.0f, 1.0f,
+                      stream);
+}
+
+int ck_kv_store_fp8(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
+                    int cache_capacity, int head_dim, float k_scale, float v_scale, void *stream) {
+    if (!scale_ok(k_scale) || !scale_ok(v_scale)) return CK_EINVAL;
+    return kv_store_q(k_cache, v_cache, k, v, pos, num_kv_heads, cache_capacity, head_dim, KV_FP8, k_scale, v_scale,
+                      stream);
+}
+
+static int attn_call(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                     int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_type, float k_scale,
+                     float v_scale, void *scratch, size_t scratch_bytes, void *stream) {
     int rc = check_ptrs({q, k_cache, v_cache, out}, {});
     if (rc) return rc;
+    if (kv_type != 0 && head_dim != 64 && head_dim != 128) return CK_EINVAL;
     if ((rc = attn_shape_ok(num_heads, num_kv_heads, head_dim))) return rc;
     if (cache_capacity <= 0) return CK_EINVAL;
     if (kv_tokens < 1 || kv_tokens > cache_capacity) return CK_ERANGE;
@@ -368,8 +423,8 @@ int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cach
     if (!st) return CK_ECUDA;
     AttnArgs a{};
     a.q = q;
-    a.k_cache = k_cache;
-    a.v_cache = v_cache;
+    a.k_cache = static_cast<const float *>(k_cache);  // elements of kv_type
+    a.v_cache = static_cast<const float *>(v_cache);
     a.kv_tokens = kv_tokens;
     a.H = num_heads;
     a.KV = num_kv_heads;
@@ -378,6 +433,9 @@ int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cach
     a.splits = S;
     a.part = static_cast<float *>(scratch);
     a.out = out;
+    a.kv_type = kv_type;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.status = st;
     return launch_attention(a, 1, as_stream(stream), false, false) ? CK_ECUDA : CK_OK;
 }

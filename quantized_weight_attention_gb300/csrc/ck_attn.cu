@@ -3,6 +3,8 @@
 // kernels of ck_attn_kernels.cuh, which are instantiated one head_dim per
 // translation unit (ck_attn_d*.cu).  Also here: the standalone RoPE and
 // KV-store kernels (STEP 5, STEP 6).
+#include <cuda_bf16.h>
+
 #include "ck_attn_kernels.cuh"
 
 namespace ck {
@@ -31,6 +33,29 @@ __global__ void k_kv_store(float *kc, float *vc, const float *__restrict__ k, co
     const size_t o = (static_cast<size_t>(h) * C + pos) * hd + d;
     kc[o] = k[idx];
     vc[o] = v[idx];
+}
+
+// KV store into a bf16 cache (round to nearest even) or an fp8 E4M3 cache
+// (the IEEE quotient x / scale, then round to nearest even onto E4M3 with
+// saturation to +-448; the value is converted into both halves of the packed
+// pair, so the byte taken does not depend on the pair's order).
+__global__ void k_kv_store_q(uint8_t *kc, uint8_t *vc, const float *__restrict__ k, const float *__restrict__ v,
+                             int pos, int KV, int C, int hd, int kv_type, float k_scale, float v_scale) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= KV * hd) return;
+    const int h = idx / hd, d = idx - h * hd;
+    const size_t o = (static_cast<size_t>(h) * C + pos) * hd + d;
+    if (kv_type == KV_BF16) {
+        reinterpret_cast<__nv_bfloat16 *>(kc)[o] = __float2bfloat16_rn(k[idx]);
+        reinterpret_cast<__nv_bfloat16 *>(vc)[o] = __float2bfloat16_rn(v[idx]);
+    } else {
+        const float xk = __fdiv_rn(k[idx], k_scale), xv = __fdiv_rn(v[idx], v_scale);
+        unsigned short pk, pv;
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pk) : "f"(xk), "f"(xk));
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pv) : "f"(xv), "f"(xv));
+        kc[o] = static_cast<uint8_t>(pk & 0xFF);
+        vc[o] = static_cast<uint8_t>(pv & 0xFF);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -64,19 +89,35 @@ int attn_splits_batched(int B, int KV, int max_tokens) {
     return S;
 }
 
-extern template int launch_attention_dpl<1>(const AttnArgs &, int, cudaStream_t, bool, bool);
-extern template int launch_attention_dpl<2>(const AttnArgs &, int, cudaStream_t, bool, bool);
-extern template int launch_attention_dpl<3>(const AttnArgs &, int, cudaStream_t, bool, bool);
-extern template int launch_attention_dpl<4>(const AttnArgs &, int, cudaStream_t, bool, bool);
-extern template int launch_attention_dpl<8>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<1, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<2, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<3, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<4, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<8, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<2, KV_BF16>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<4, KV_BF16>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<2, KV_FP8>(const AttnArgs &, int, cudaStream_t, bool, bool);
+extern template int launch_attention_dpl<4, KV_FP8>(const AttnArgs &, int, cudaStream_t, bool, bool);
 
 int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
+    if (a.kv_type == KV_BF16 || a.kv_type == KV_FP8) {  // head_dim 64 and 128
+        const bool f8 = a.kv_type == KV_FP8;
+        switch (a.hd) {
+            case 64:
+                return f8 ? launch_attention_dpl<2, KV_FP8>(a, B, s, pdl_first, pdl_combine)
+                          : launch_attention_dpl<2, KV_BF16>(a, B, s, pdl_first, pdl_combine);
+            case 128:
+                return f8 ? launch_attention_dpl<4, KV_FP8>(a, B, s, pdl_first, pdl_combine)
+                          : launch_attention_dpl<4, KV_BF16>(a, B, s, pdl_first, pdl_combine);
+            default: return -1;
+        }
+    }
     switch (a.hd / 32) {
-        case 1: return launch_attention_dpl<1>(a, B, s, pdl_first, pdl_combine);
-        case 2: return launch_attention_dpl<2>(a, B, s, pdl_first, pdl_combine);
-        case 3: return launch_attention_dpl<3>(a, B, s, pdl_first, pdl_combine);
-        case 4: return launch_attention_dpl<4>(a, B, s, pdl_first, pdl_combine);
-        case 8: return launch_attention_dpl<8>(a, B, s, pdl_first, pdl_combine);
+        case 1: return launch_attention_dpl<1, KV_F32>(a, B, s, pdl_first, pdl_combine);
+        case 2: return launch_attention_dpl<2, KV_F32>(a, B, s, pdl_first, pdl_combine);
+        case 3: return launch_attention_dpl<3, KV_F32>(a, B, s, pdl_first, pdl_combine);
+        case 4: return launch_attention_dpl<4, KV_F32>(a, B, s, pdl_first, pdl_combine);
+        case 8: return launch_attention_dpl<8, KV_F32>(a, B, s, pdl_first, pdl_combine);
         default: return -1;
     }
 }
@@ -85,6 +126,14 @@ int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, in
     const int n = (H + KV) * (hd / 2);
     if (n == 0) return 0;
     k_rope<<<(n + 255) / 256, 256, 0, s>>>(q, k, c, sn, pos, H, KV, hd);
+    return cudaGetLastError() == cudaSuccess ? 0 : -5;
+}
+
+int launch_kv_store_q(void *kc, void *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
+                      int kv_type, float k_scale, float v_scale, cudaStream_t s) {
+    const int n = KV * hd;
+    k_kv_store_q<<<(n + 255) / 256, 256, 0, s>>>(static_cast<uint8_t *>(kc), static_cast<uint8_t *>(vc), k, v, pos,
+                                                 KV, C, hd, kv_type, k_scale, v_scale);
     return cudaGetLastError() == cudaSuccess ? 0 : -5;
 }
 

@@ -2,5 +2,5 @@
 #include "ck_attn_kernels.cuh"
 
 namespace ck {
-template int launch_attention_dpl<8>(const AttnArgs &, int, cudaStream_t, bool, bool);
+template int launch_attention_dpl<8, KV_F32>(const AttnArgs &, int, cudaStream_t, bool, bool);
 }  // namespace ck

@@ -46,35 +46,86 @@ constexpr int GMAX = 8;                              // query heads per KV head
 // the slot's phase p - 1 and the parity wait can never pass on a stale phase.
 constexpr int AT_RING_BYTES = 192 * 1024;
 constexpr int AT_MAX_SLOTS = 48;
-// Large-stage height: the largest power-of-two multiple of 8 rows with at
-// most 16 KB per operand (tiles per stage a power of two: shifts, not
-// divisions, in the consumer loop).
-__host__ __device__ constexpr int at_rs_big(int hd) {
-    return hd * 4 * 128 <= 16384 ? 128 : hd * 4 * 64 <= 16384 ? 64 : hd * 4 * 32 <= 16384 ? 32 : hd * 4 * 16 <= 16384 ? 16 : 8;
+// Cache element types (KV_F32, KV_BF16, KV_FP8 of ck_internal.h); es =
+// bytes per element.
+__host__ __device__ constexpr int kv_es(int kt) { return kt == KV_F32 ? 4 : kt == KV_BF16 ? 2 : 1; }
+// Stage heights: the largest power-of-two multiple of 8 rows (at most 128)
+// with at most `bytes` per operand (tiles per stage a power of two: shifts,
+// not divisions, in the consumer loop).  Large stages: 16 KB per operand;
+// short splits: 8 rows of fp32, ~4 KB of bf16 or fp8 (16 or 32 rows at hd 128).
+__host__ __device__ constexpr int at_rows_for(int hd, int es, int bytes) {
+    return hd * es * 128 <= bytes ? 128 : hd * es * 64 <= bytes ? 64 : hd * es * 32 <= bytes ? 32
+           : hd * es * 16 <= bytes ? 16 : 8;
 }
+__host__ __device__ constexpr int at_rs_big(int hd, int es = 4) { return at_rows_for(hd, es, 16384); }
 // Ring geometry of the two stage heights (compile-time constants in each
 // kernel instantiation: the consumer loop stays as lean as with fixed tiles).
-__host__ __device__ constexpr int at_rs(int hd, bool big) { return big ? at_rs_big(hd) : AT_TILE; }
-__host__ __device__ constexpr int at_ss_bytes(int hd, bool big) { return 2 * at_rs(hd, big) * hd * 4; }
-__host__ __device__ constexpr int at_nss_from(int hd, bool big, int n) {
-    return n <= 1 ? 1 : ((at_rs(hd, big) / AT_TILE * n) % AT_CONSUMERS == 0 ? n : at_nss_from(hd, big, n - 1));
+__host__ __device__ constexpr int at_rs(int hd, bool big, int es = 4) {
+    return big ? at_rs_big(hd, es) : es == 4 ? AT_TILE : at_rows_for(hd, es, 4096);
 }
-__host__ __device__ constexpr int at_nss(int hd, bool big) {
-    return at_nss_from(hd, big, AT_RING_BYTES / at_ss_bytes(hd, big) > AT_MAX_SLOTS ? AT_MAX_SLOTS
-                                                                                    : AT_RING_BYTES / at_ss_bytes(hd, big));
+__host__ __device__ constexpr int at_ss_bytes(int hd, bool big, int es = 4) { return 2 * at_rs(hd, big, es) * hd * es; }
+__host__ __device__ constexpr int at_nss_from(int hd, bool big, int n, int es = 4) {
+    return n <= 1 ? 1
+                  : ((at_rs(hd, big, es) / AT_TILE * n) % AT_CONSUMERS == 0 ? n : at_nss_from(hd, big, n - 1, es));
 }
-// stages in flight: ~96 KB of large stages, ~80 KB of 8-row stages
-__host__ __device__ constexpr int at_la(int hd, bool big) {
-    return ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big) < 1 ? 1
-           : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big) > at_nss(hd, big) - 1
-               ? at_nss(hd, big) - 1
-               : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big);
+__host__ __device__ constexpr int at_nss(int hd, bool big, int es = 4) {
+    return at_nss_from(hd, big,
+                       AT_RING_BYTES / at_ss_bytes(hd, big, es) > AT_MAX_SLOTS ? AT_MAX_SLOTS
+                                                                              : AT_RING_BYTES / at_ss_bytes(hd, big, es),
+                       es);
+}
+// stages in flight: ~96 KB of large stages, ~80 KB of short-split stages
+__host__ __device__ constexpr int at_la(int hd, bool big, int es = 4) {
+    return ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big, es) < 1 ? 1
+           : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big, es) > at_nss(hd, big, es) - 1
+               ? at_nss(hd, big, es) - 1
+               : ((big ? 96 : 80) * 1024) / at_ss_bytes(hd, big, es);
 }
 // Large stages for splits of at least 8 of them.
-__host__ __device__ inline bool at_big(int hd, int chunk_rows) { return chunk_rows >= 8 * at_rs_big(hd); }
+__host__ __device__ inline bool at_big(int hd, int chunk_rows, int es = 4) { return chunk_rows >= 8 * at_rs_big(hd, es); }
 static_assert(at_nss(32, true) >= 2 && at_nss(96, true) >= 2 && at_nss(128, true) >= 2 && at_nss(256, true) >= 2 &&
                   at_nss(32, false) >= 2 && at_nss(256, false) >= 2,
               "stage ring");
+static_assert(at_rs(128, false) == AT_TILE && at_rs_big(128) == 32, "fp32 stage heights");
+static_assert(at_nss(64, true, 2) >= 2 && at_nss(128, true, 2) >= 2 && at_nss(64, false, 2) >= 2 &&
+                  at_nss(128, false, 2) >= 2 && at_nss(64, true, 1) >= 2 && at_nss(128, true, 1) >= 2 &&
+                  at_nss(64, false, 1) >= 2 && at_nss(128, false, 1) >= 2,
+              "stage ring (bf16, fp8)");
+
+// Four (two) consecutive cache elements as fp32, exactly: bf16 by moving its
+// bits into the high half of an fp32 word, E4M3 through the hardware
+// conversion to fp16 pairs.
+template <int KT>
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<unsigned short>(two & 0xFFFFu)));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+template <int KT>
+__device__ __forceinline__ float4 kv_load4(const uint8_t *p) {
+    if constexpr (KT == KV_F32) {
+        return *reinterpret_cast<const float4 *>(p);
+    } else if constexpr (KT == KV_BF16) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                           __uint_as_float(u.y & 0xFFFF0000u));
+    } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        const float2 lo = e4m3x2_to_float2<KT>(u), hi = e4m3x2_to_float2<KT>(u >> 16);
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+}
+template <int KT>
+__device__ __forceinline__ float2 kv_load2(const uint8_t *p) {
+    if constexpr (KT == KV_F32) {
+        return *reinterpret_cast<const float2 *>(p);
+    } else if constexpr (KT == KV_BF16) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p);
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        return e4m3x2_to_float2<KT>(*reinterpret_cast<const uint16_t *>(p));
+    }
+}
 
 // P row stride (floats): G heads, each duplicated into a pair, padded so
 // rows stay 16-byte aligned.
@@ -158,8 +209,9 @@ __device__ __forceinline__ void reduce_scatter_heads(float (&v)[8][R], int slice
 // j's softmax state.
 // PV: lane = dims; each row adds p_j * v to GT accumulators, two dims per
 // packed FMA.
-template <int DPL, int GT, bool BIG>
+template <int DPL, int GT, bool BIG, int KT>
 __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) {
+    constexpr int ES = kv_es(KT);
     constexpr int HD = 32 * DPL;
     constexpr int HD4 = HD / 4;
     constexpr int VEC = (DPL % 4 == 0) ? 4 : ((DPL % 2 == 0) ? 2 : 1);
@@ -170,7 +222,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.off_full);
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.off_empty);
     uint64_t *qbar = reinterpret_cast<uint64_t *>(smem + L.off_qbar);
-    float *stage = reinterpret_cast<float *>(smem + L.off_stage);
+    uint8_t *stage = smem + L.off_stage;  // cache elements of ES bytes
     float *qs = reinterpret_cast<float *>(smem + L.off_q);
 
     const int s = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -217,10 +269,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         }
         return;
     }
-    const float *kc = (a.k_caches ? a.k_caches[b] : a.k_cache) + static_cast<size_t>(g) * a.C * HD;
-    const float *vc = (a.v_caches ? a.v_caches[b] : a.v_cache) + static_cast<size_t>(g) * a.C * HD;
+    const uint8_t *kc = reinterpret_cast<const uint8_t *>(a.k_caches ? a.k_caches[b] : a.k_cache) +
+                        static_cast<size_t>(g) * a.C * HD * ES;
+    const uint8_t *vc = reinterpret_cast<const uint8_t *>(a.v_caches ? a.v_caches[b] : a.v_cache) +
+                        static_cast<size_t>(g) * a.C * HD * ES;
     const int ntiles = (t1 - t0 + AT_TILE - 1) / AT_TILE;
-    constexpr int RS = at_rs(HD, BIG), TPS = RS / AT_TILE, NSS = at_nss(HD, BIG), LA = at_la(HD, BIG);
+    constexpr int RS = at_rs(HD, BIG, ES), TPS = RS / AT_TILE, NSS = at_nss(HD, BIG, ES), LA = at_la(HD, BIG, ES);
 
     if (threadIdx.x < NSS) {  // one barrier pair per thread: a serial loop costs ~0.5 us
         mbar_init(&full[threadIdx.x], 1);
@@ -250,11 +304,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
                 const int r = t0 + k * RS;
                 const int n = min(RS, t1 - r);
                 if (r + n >= T) pdl_wait();
-                float *dst = stage + static_cast<size_t>(sl) * 2 * RS * HD;
-                const uint32_t bytes = static_cast<uint32_t>(n) * HD * 4;
+                uint8_t *dst = stage + static_cast<size_t>(sl) * 2 * RS * HD * ES;
+                const uint32_t bytes = static_cast<uint32_t>(n) * HD * ES;
                 mbar_arrive_expect_tx(&full[sl], 2 * bytes);
-                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD, bytes, &full[sl]);
-                bulk_g2s(dst + RS * HD, vc + static_cast<size_t>(r) * HD, bytes, &full[sl]);
+                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
+                bulk_g2s(dst + RS * HD * ES, vc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
             }
         }
         return;
@@ -276,7 +330,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     if (!mbar_wait(qbar, 0)) flag_error(a.status, FLAG_TIMEOUT);
     consumers_sync();
 
-    const float scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    float scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
+    if constexpr (KT == KV_FP8) scale2 *= a.k_scale;  // k = code * k_scale
     const float4 *q4 = reinterpret_cast<const float4 *>(qs);
     const int slice = lane & 7, rl = lane >> 3;
     float mrun = -INFINITY, lrun = 0.0f;  // head `slice`
@@ -293,13 +348,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     for (int t = cw; t < ntiles; t += AT_CONSUMERS) {
         const int k = t / TPS, st = k % NSS;
         if (!mbar_wait(&full[st], (k / NSS) & 1)) flag_error(a.status, FLAG_TIMEOUT);
-        const float *Kt = stage + static_cast<size_t>(st) * 2 * RS * HD + (t - k * TPS) * AT_TILE * HD;
-        const float *Vt = Kt + RS * HD;
+        const uint8_t *Kt = stage + (static_cast<size_t>(st) * 2 * RS * HD + (t - k * TPS) * AT_TILE * HD) * ES;
+        const uint8_t *Vt = Kt + RS * HD * ES;
         const int n = min(AT_TILE, t1 - (t0 + t * AT_TILE));
 
         // ---- scores, rows rl + 4k, in passes of k = {2p, 2p + 1}
         float my[AT_RPL];
-        const float4 *K4 = reinterpret_cast<const float4 *>(Kt);
 #pragma unroll
         for (int pass = 0; pass < AT_RPL / 2; ++pass) {
             float2 sp[GT][2];
@@ -311,7 +365,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
             for (int c = 0; c < DPL; ++c) {
                 float4 kk[2];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) kk[k] = K4[(rl + 4 * (2 * pass + k)) * HD4 + slice + 8 * c];
+                for (int k = 0; k < 2; ++k)
+                    kk[k] = kv_load4<KT>(Kt + ((rl + 4 * (2 * pass + k)) * HD + 4 * (slice + 8 * c)) * ES);
 #pragma unroll
                 for (int j = 0; j < GT; ++j) {
                     const float4 qv = q4[j * HD4 + slice + 8 * c];
@@ -384,13 +439,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
                 float2 vv[DPL / 2];
 #pragma unroll
                 for (int u = 0; u < NV; ++u) {
-                    const float *src = Vt + r * HD + VEC * (lane + 32 * u);
+                    const uint8_t *src = Vt + (r * HD + VEC * (lane + 32 * u)) * ES;
                     if constexpr (VEC == 4) {
-                        const float4 tv = *reinterpret_cast<const float4 *>(src);
+                        const float4 tv = kv_load4<KT>(src);
                         vv[2 * u] = make_float2(tv.x, tv.y);
                         vv[2 * u + 1] = make_float2(tv.z, tv.w);
                     } else {
-                        vv[u] = *reinterpret_cast<const float2 *>(src);
+                        vv[u] = kv_load2<KT>(src);
                     }
                 }
 #pragma unroll
@@ -399,8 +454,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
                     for (int e = 0; e < DPL / 2; ++e) acc[j][e] = __ffma2_rn(pp[j], vv[e], acc[j][e]);
             } else {
                 float vv[DPL];
+                static_assert(KT == KV_F32 || DPL % 2 == 0, "bf16 / fp8 caches: head_dim a multiple of 64");
 #pragma unroll
-                for (int u = 0; u < DPL; ++u) vv[u] = Vt[r * HD + lane + 32 * u];
+                for (int u = 0; u < DPL; ++u) vv[u] = reinterpret_cast<const float *>(Vt)[r * HD + lane + 32 * u];
 #pragma unroll
                 for (int j = 0; j < GT; ++j)
 #pragma unroll
@@ -423,7 +479,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         mlw[(AT_CONSUMERS + cw) * GMAX + slice] = lrun;
     }
     consumers_sync();  // every tile consumed: the ring is idle
-    float *accw = stage;  // [NC][G][HD]
+    float *accw = reinterpret_cast<float *>(stage);  // [NC][G][HD]
 #pragma unroll
     for (int j = 0; j < GT; ++j) {
         if (j < G) {
@@ -471,6 +527,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         for (int w = 0; w < AT_CONSUMERS; ++w) {
             if (mlw[w * GMAX + j] != -INFINITY) t = fmaf(scw[w * GMAX + j], accw[(w * G + j) * HD + (idx - j * HD)], t);
         }
+        if constexpr (KT == KV_FP8) t *= a.v_scale;  // v = code * v_scale
         rec[2 * G + idx] = t;
     }
 }
@@ -644,15 +701,16 @@ __global__ void __launch_bounds__(256) k_attn_combine_w(const AttnArgs a, int B)
     combine_store<HD>(a, b, h, blk, lane, __fdiv_rn(t, L));
 }
 
-template <int DPL, int GT>
+template <int DPL, int GT, int KT>
 static int launch_attn_gt(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
     AttnArgs a = a0;
     const AttnSmem L = attn_smem(32 * DPL);
     // stage height from the longest split (all splits of a launch share the plan)
     const int T = a.d_pos ? a.C : a.kv_tokens;
     const int chunk = a.chunk > 0 ? a.chunk : (T + a.splits - 1) / a.splits;
-    const void *fs = at_big(32 * DPL, chunk) ? reinterpret_cast<const void *>(k_attn_split<DPL, GT, true>)
-                                              : reinterpret_cast<const void *>(k_attn_split<DPL, GT, false>);
+    const void *fs = at_big(32 * DPL, chunk, kv_es(KT))
+                         ? reinterpret_cast<const void *>(k_attn_split<DPL, GT, true, KT>)
+                         : reinterpret_cast<const void *>(k_attn_split<DPL, GT, false, KT>);
     ensure_smem(fs, L.total);
     void *args1[] = {&a};
     cudaError_t e = launch(fs, dim3(a.splits, a.KV, B), dim3(AT_THREADS), L.total, s, pdl_first, args1);
@@ -671,18 +729,18 @@ static int launch_attn_gt(const AttnArgs &a0, int B, cudaStream_t s, bool pdl_fi
 }
 
 // Query groups of 1, 2, 4, 7 and 8 heads run exact kernels; 3, 5 and 6 run
-// in the next larger one with the extra heads masked.
-template <int DPL>
+// in the next larger one with the extra heads masked.  KT: cache element type.
+template <int DPL, int KT>
 int launch_attention_dpl(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
     switch (a.H / a.KV) {
-        case 1: return launch_attn_gt<DPL, 1>(a, B, s, pdl_first, pdl_combine);
-        case 2: return launch_attn_gt<DPL, 2>(a, B, s, pdl_first, pdl_combine);
+        case 1: return launch_attn_gt<DPL, 1, KT>(a, B, s, pdl_first, pdl_combine);
+        case 2: return launch_attn_gt<DPL, 2, KT>(a, B, s, pdl_first, pdl_combine);
         case 3:
-        case 4: return launch_attn_gt<DPL, 4>(a, B, s, pdl_first, pdl_combine);
+        case 4: return launch_attn_gt<DPL, 4, KT>(a, B, s, pdl_first, pdl_combine);
         case 5:
         case 6:
-        case 7: return launch_attn_gt<DPL, 7>(a, B, s, pdl_first, pdl_combine);
-        case 8: return launch_attn_gt<DPL, 8>(a, B, s, pdl_first, pdl_combine);
+        case 7: return launch_attn_gt<DPL, 7, KT>(a, B, s, pdl_first, pdl_combine);
+        case 8: return launch_attn_gt<DPL, 8, KT>(a, B, s, pdl_first, pdl_combine);
         default: return -1;
     }
 }

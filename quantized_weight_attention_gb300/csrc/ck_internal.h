@@ -106,6 +106,9 @@ int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl
 void plan_qkv(QkvArgs &a);
 
 // ---- attention (ck_attn.cu) ----
+// Cache element types: fp32 (the layer's cache), bf16, fp8 E4M3 (with
+// per-tensor scales).
+constexpr int KV_F32 = 0, KV_BF16 = 1, KV_FP8 = 2;
 struct AttnArgs {
     const float *q;           // [B][H*hd]
     const float *k_cache;     // single sequence: the cache; batched: unused
@@ -125,6 +128,8 @@ struct AttnArgs {
     int img_groups;           // its sequence groups: img_groups(B)
     const void *l2_prefetch;  // optional: bytes the next kernel reads, pulled into L2
     size_t l2_prefetch_bytes;
+    int kv_type;              // cache elements: 0 fp32, 1 bf16, 2 fp8 E4M3 (k_cache / v_cache hold them)
+    float k_scale, v_scale;   // fp8: k = code * k_scale, v = code * v_scale
     unsigned *status;
 };
 size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
@@ -134,5 +139,9 @@ int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, b
 int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, int H, int KV, int hd, cudaStream_t s);
 int launch_kv_store(float *kc, float *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
                     cudaStream_t s);
+// The same into a bf16 cache (round to nearest even) or an fp8 E4M3 cache
+// (code = E4M3(x / scale), round to nearest even, saturated to +-448).
+int launch_kv_store_q(void *kc, void *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
+                      int kv_type, float k_scale, float v_scale, cudaStream_t s);
 
 }  // namespace ck
