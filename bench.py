@@ -45,7 +45,10 @@ def parse():
     p.add_argument("--steps", type=int, default=60000)
     p.add_argument("--warmup", type=int, default=600)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="7b8k", choices=["tiny", "small1k", "7b8k", "stack32k", "batched64"])
+    p.add_argument("--config", default="7b8k",
+                   choices=["tiny", "small1k", "7b8k", "stack32k", "batched64", "attn32k"])
+    p.add_argument("--kv-dtype", default="bf16", choices=["f32", "bf16", "fp8"],
+                   help="attn32k: cache element type (fp8 = E4M3 with per-tensor scales)")
     p.add_argument("--layers", type=int, default=0, help="stack32k: layers in the stack (default: all 28)")
     p.add_argument("--kv-cap", type=int, default=0,
                    help="batched64: cap every cache at this many rows (a small case for profilers; not the workload)")
@@ -214,6 +217,8 @@ def run_ours(args, ws, rank, local, pg):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.config == "attn32k":
+        return run_attn_kv(args, ws, pg, torch, q, synth, dev)
     w = synth.WORKLOADS[args.config]
     if args.config == "stack32k":
         return run_stack(args, ws, pg, torch, q, synth, dev)
@@ -437,6 +442,157 @@ def run_stack(args, ws, pg, torch, q, synth, dev):
             "gpu_launches": launches_per_layer(w) * nlayers * K, "clocks": clocks}
 
 
+KV_ES = {"f32": 4, "bf16": 2, "fp8": 1}
+ATTN_ROWS = 32769  # the 32K-context attention of the 7B-shaped layer (pos 32768)
+
+
+def attn_kv_shape(synth):
+    w = synth.WORKLOADS["7b8k"]
+    return w.H, w.KV, w.hd, ATTN_ROWS, ATTN_ROWS + 63
+
+
+def run_attn_kv(args, ws, pg, torch, q, synth, dev):
+    """The decode attention of the 7B-shaped layer at 32,769 rows over an fp32,
+    bf16 or fp8 E4M3 cache: one C-ABI attention call per step, calls back to
+    back in a CUDA graph over replicated caches (more bytes than L2)."""
+    H, KV, hd, Tn, C = attn_kv_shape(synth)
+    dt, es = args.kv_dtype, KV_ES[args.kv_dtype]
+    kv_bytes = 2 * KV * Tn * hd * es
+    per_rep = 2 * KV * C * hd * es
+    R = max(3, -(-int(2.5 * L2_BYTES) // per_rep))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    ks = vs = 0.01
+    reps = []
+    for r in range(R):
+        if dt == "fp8":  # finite E4M3 codes, random sign
+            mk = lambda: (torch.randint(0, 0x7F, (KV, C, hd), generator=gen, device=dev, dtype=torch.int32) |
+                          (torch.randint(0, 2, (KV, C, hd), generator=gen, device=dev, dtype=torch.int32) << 7)
+                          ).to(torch.uint8)
+        else:
+            f = torch.float32 if dt == "f32" else torch.bfloat16
+            mk = lambda: torch.randn((KV, C, hd), generator=gen, device=dev, dtype=torch.float32).to(f)
+        reps.append((mk(), mk()))
+    qv = torch.randn(H * hd, generator=gen, device=dev, dtype=torch.float32)
+    out = torch.empty(H * hd, dtype=torch.float32, device=dev)
+    nbytes = q.ck_attn_scratch_size(H, KV, C, hd)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i, qin=None, o=None):
+        kc, vc = reps[i % R]
+        qq = qv if qin is None else qin
+        oo = out if o is None else o
+        if dt == "f32":
+            return q.ck_attn_decode_gqa(qq, kc, vc, oo, H, KV, Tn, C, hd, scratch, nbytes, stream.cuda_stream)
+        if dt == "bf16":
+            return q.ck_attn_decode_gqa_bf16(qq, kc, vc, oo, H, KV, Tn, C, hd, scratch, nbytes, stream.cuda_stream)
+        return q.ck_attn_decode_gqa_fp8(qq, kc, vc, oo, H, KV, Tn, C, hd, ks, vs, scratch, nbytes,
+                                        stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(R):
+            q.check(call(i))
+    torch.cuda.synchronize()
+    n_g = 4 * R
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_g):
+            q.check(call(i))
+    K = max(1, -(-args.steps // n_g)) * n_g  # whole graph replays
+    K = min(K, 40 * n_g)
+    W = max(args.warmup, 3)
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // n_g)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // n_g):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    ach = kv_bytes * ws * K / sec / 1e9
+    peak, peak_kind = measured_peaks()
+    # e2e: q from pinned host memory, the output back, every call
+    Ke = min(K, 2000)
+    qh = qv.cpu().pin_memory()
+    oh = torch.empty(H * hd, dtype=torch.float32).pin_memory()
+    qd = torch.empty_like(qv)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(Ke):
+            qd.copy_(qh, non_blocking=True)
+            q.check(call(i, qd))
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1))
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    line = {"metric": "decode attention calls/s and achieved HBM GB/s vs GB300 peak", "value": round(ws * K / sec, 1),
+            "unit": "attention-calls/s", "n_gpus": ws, "steps": K, "warmup": W, "ms_per_step": round(ms / K, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f32": "f32", "bf16": "bf16 cache, f32 math", "fp8": "fp8 e4m3 cache, f32 math"}[dt],
+            "data": "synthetic",
+            "config": {"workload": f"attn32k: decode attention of the 28/4-head hd 128 layer over {Tn} rows of a "
+                                   f"{dt} cache (fp8: per-tensor scales {ks}, {vs}), one C-ABI call per step",
+                       "l2": f"inputs larger than L2: {R} cache replicas rotated "
+                             f"({R * per_rep / 2**20:.0f} MiB)"},
+            "step_hbm_gbs": round(ach, 1), "step_bytes": kv_bytes,
+            "roofline": {"kernel": "attention (split + combine, one call)", "bound": "hbm", "achieved": round(ach, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                         "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None},
+            "e2e": {"value": round(ws * Ke / (e2e_ms / 1e3), 1), "unit": "attention-calls/s",
+                    "h2d_bytes_per_step": H * hd * 4, "d2h_bytes_per_step": H * hd * 4, "steps": Ke,
+                    "how": "per call: pinned q -> device, the attention call, out -> pinned host"},
+            "gpu_launches": 2 * K, "clocks": clocks}
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        line["cpu_baseline"] = cpu_baseline_attn(synth, dt, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_attn(synth, dt, budget_s):
+    """The oracle attention over the same shape and cache type, calls until the budget."""
+    import oracle
+    oracle.lib()
+    H, KV, hd, Tn, C = attn_kv_shape(synth)
+    rng = np.random.default_rng(7)
+    qv = rng.standard_normal(H * hd).astype(np.float32)
+    if dt == "fp8":
+        kc = (rng.integers(0, 0x7F, (KV, C, hd)) | (rng.integers(0, 2, (KV, C, hd)) << 7)).astype(np.uint8)
+        vc = kc[::-1].copy()
+    else:
+        k = rng.standard_normal((KV, C, hd)).astype(np.float32)
+        kc = oracle.bf16_from_f32(k) if dt == "bf16" else k
+        vc = kc[::-1].copy()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        if dt == "f32":
+            oracle.attention(qv, kc, vc, H, KV, Tn, C, hd)
+        else:
+            oracle.attention_kvq(qv, kc, vc, H, KV, Tn, C, hd, oracle.KV_BF16 if dt == "bf16" else oracle.KV_FP8,
+                                 0.01, 0.01)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(n / el, 4), "unit": "attention-calls/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} full attention calls ({Tn} rows, {dt} cache) by the single-threaded C oracle, "
+                      f"{el:.1f} s, cpu: {cpu_model()}"}
+
+
 def run_batched(args, ws, pg, torch, q, synth, dev):
     """64 sequences of the 7B-shaped layer with ragged caches (lengths uniform
     in [512, 16384]): one ck_decode_layer_batched call per step."""
@@ -620,6 +776,15 @@ def cpu_baseline(w, budget_s):
 
 def run_reference(args, ws):
     from quantized_weight_attention_gb300 import synth
+    if args.config == "attn32k":  # the oracle attention, as the CPU baseline
+        cb = cpu_baseline_attn(synth, args.kv_dtype, 60.0)
+        return {"impl": "reference", "metric": "decode attention calls/s and achieved HBM GB/s vs GB300 peak",
+                "value": cb["value"], "unit": "attention-calls/s", "n_gpus": ws, "steps": 1, "warmup": 0,
+                "ms_per_step": round(1e3 / cb["value"], 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64 accumulation (C oracle)", "data": "synthetic",
+                "config": {"workload": f"attn32k, {args.kv_dtype} cache (same as the GPU arm)"},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "attention-calls/s",
+                                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     w = synth.WORKLOADS[args.config]
     if args.config == "batched64":  # the oracle sequence after sequence, within a few minutes
         rng = np.random.Generator(np.random.PCG64(w.seed))
