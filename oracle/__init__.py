@@ -80,6 +80,7 @@ def lib():
             L.ref_e4m3_to_f32_n.argtypes = [P, P, ctypes.c_long]
             L.ref_attention_kvq.argtypes = [P, P, P, P, i, i, i, i, i, i, f, f]
             L.ref_kv_store_kvq.argtypes = [P, P, P, P, i, i, i, i, i, f, f]
+            L.ref_attention_paged.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, i, f, f]
             L.ref_rmsnorm.restype = f
             L.ref_rmsnorm.argtypes = [P, P, P, i, f]
             L.ref_rope.argtypes = [P, P, P, P, i, i, i, i]
@@ -264,6 +265,22 @@ def kv_store_kvq(k_cache, v_cache, k, v, pos: int, KV: int, capacity: int, hd: i
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
     lib().ref_kv_store_kvq(_p(k_cache), _p(v_cache), _p(_f32(k)), _p(_f32(v)), pos, KV, capacity, hd, kind,
                            float(k_scale), float(v_scale))
+
+
+def attention_paged(q, k_pool, v_pool, block_tables, seq_lens, B: int, H: int, KV: int, hd: int, block_size: int,
+                    max_blocks: int, window: int, kind: int = 0, k_scale: float = 1.0,
+                    v_scale: float = 1.0) -> np.ndarray:
+    """Paged decode attention: pools [num_blocks, KV, block_size, hd] of fp32 (kind 0), bf16 (1) or E4M3 (2);
+    block_tables int32 [B, max_blocks]; seq_lens int32 [B]; window 0 = all rows."""
+    dt = {0: np.float32, 1: np.uint16, 2: np.uint8}[kind]
+    kp = np.ascontiguousarray(k_pool, dt)
+    vp = np.ascontiguousarray(v_pool, dt)
+    bt = np.ascontiguousarray(block_tables, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    out = np.empty(B * H * hd, np.float32)
+    lib().ref_attention_paged(_p(_f32(q)), _p(kp), _p(vp), _p(out), _p(bt), _p(sl), B, H, KV, hd, block_size,
+                              max_blocks, window, kind, float(k_scale), float(v_scale))
+    return out
 
 
 def decode_layer(x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos, rope_sin,

@@ -502,6 +502,69 @@ void ref_kv_store_kvq(void *k_cache, void *v_cache, const float *k, const float 
 }
 
 /* ------------------------------------------------------------------------
+ * Paged decode attention with a sliding window (page "paged decode
+ * attention": paged_decode_attn_bf16 / _fp8 and their GQA forms; only the
+ * launchers are printed).  Readings: the pools are [num_blocks][KV]
+ * [block_size][hd]; row t of sequence b is row t % block_size of physical
+ * block block_tables[b * max_blocks + t / block_size]; the sequence attends
+ * rows [T0, T) with T = seq_lens[b] and T0 = max(0, T - window) when
+ * window > 0, else 0; the attention is ref_attention's on those rows.
+ * kind: 0 fp32, 1 bf16, 2 E4M3 (values as in ref_attention_kvq).
+ * ---------------------------------------------------------------------- */
+static double pool_value(const void *pool, size_t i, int kind, double scale)
+{
+    if (kind == 0)
+        return (double)((const float *)pool)[i];
+    return kvq_value(pool, i, kind, scale);
+}
+
+void ref_attention_paged(const float *q, const void *k_pool, const void *v_pool, float *out,
+                         const int32_t *block_tables, const int32_t *seq_lens, int B, int H, int KV, int hd,
+                         int block_size, int max_blocks, int window, int kind, float k_scale, float v_scale)
+{
+    const double scale = 1.0 / sqrt((double)hd);
+    for (int b = 0; b < B; ++b) {
+        const int T = seq_lens[b];
+        const int T0 = (window > 0 && T > window) ? T - window : 0;
+        const int n = T - T0;
+        double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        double *o = (double *)malloc(sizeof(double) * (size_t)hd);
+        for (int h = 0; h < H; ++h) {
+            const int kvh = (int)((long)h * KV / H);
+            const float *qh = q + ((size_t)b * H + h) * hd;
+            double m = -INFINITY;
+            for (int t = T0; t < T; ++t) {
+                const int pb = block_tables[(size_t)b * max_blocks + t / block_size];
+                const size_t base = (((size_t)pb * KV + kvh) * block_size + t % block_size) * hd;
+                double dot = 0.0;
+                for (int d = 0; d < hd; ++d)
+                    dot += (double)qh[d] * pool_value(k_pool, base + d, kind, k_scale);
+                s[t - T0] = dot * scale;
+                if (s[t - T0] > m)
+                    m = s[t - T0];
+            }
+            double l = 0.0;
+            for (int i = 0; i < n; ++i) {
+                s[i] = exp(s[i] - m);
+                l += s[i];
+            }
+            for (int d = 0; d < hd; ++d)
+                o[d] = 0.0;
+            for (int t = T0; t < T; ++t) {
+                const int pb = block_tables[(size_t)b * max_blocks + t / block_size];
+                const size_t base = (((size_t)pb * KV + kvh) * block_size + t % block_size) * hd;
+                for (int d = 0; d < hd; ++d)
+                    o[d] += s[t - T0] * pool_value(v_pool, base + d, kind, v_scale);
+            }
+            for (int d = 0; d < hd; ++d)
+                out[((size_t)b * H + h) * hd + d] = n > 0 ? (float)(o[d] / l) : 0.0f;
+        }
+        free(s);
+        free(o);
+    }
+}
+
+/* ------------------------------------------------------------------------
  * mega_fused_attention_decode_q5_0, in the page's order (STEP 1 .. STEP 8).
  * `dbg_*` are optional (NULL-able) taps of the intermediates:
  *   dbg_xq   [D/32 Q8_0 blocks]   the quantized normed input

@@ -131,3 +131,66 @@ def test_kv_store_kvq_writes_only_row_pos(kind):
     assert np.array_equal(kc[:, pos].ravel(), enc(k, 0.01)) and np.array_equal(vc[:, pos].ravel(), enc(v, 0.02))
     rest = [t for t in range(C) if t != pos]
     assert np.array_equal(kc[:, rest], k0[:, rest]) and np.array_equal(vc[:, rest], v0[:, rest])
+
+
+def _pool_from_contiguous(cache, block_size, perm):
+    """cache [KV, C, hd] -> pool [num_blocks, KV, block_size, hd] with logical block i at physical perm[i]."""
+    KV, C, hd = cache.shape
+    nb = C // block_size
+    pool = np.zeros((len(perm), KV, block_size, hd), cache.dtype)
+    for i in range(nb):
+        pool[perm[i]] = cache[:, i * block_size:(i + 1) * block_size].transpose(0, 1, 2)
+    return pool
+
+
+def test_paged_attention_with_identity_table_equals_contiguous():
+    rng = np.random.default_rng(21)
+    H, KV, hd, bs, nb = 8, 2, 64, 16, 6
+    C = bs * nb
+    q = rng.standard_normal(H * hd).astype(np.float32)
+    k = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    v = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    perm = np.arange(nb)
+    kp, vp = _pool_from_contiguous(k, bs, perm), _pool_from_contiguous(v, bs, perm)
+    for T in (1, 15, 16, 17, 90, 96):
+        got = oracle.attention_paged(q, kp, vp, perm[None, :], [T], 1, H, KV, hd, bs, nb, 0)
+        assert np.array_equal(got, oracle.attention(q, k, v, H, KV, T, C, hd)), T
+
+
+def test_paged_attention_is_invariant_to_block_placement():
+    rng = np.random.default_rng(22)
+    H, KV, hd, bs, nb = 4, 2, 64, 32, 5
+    C = bs * nb
+    q = rng.standard_normal(2 * H * hd).astype(np.float32)
+    k = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    v = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    ident = np.arange(nb)
+    perm = rng.permutation(2 * nb)[:nb]  # a pool twice as large, blocks scattered
+    kp1, vp1 = _pool_from_contiguous(k, bs, ident), _pool_from_contiguous(v, bs, ident)
+    kp2 = np.zeros((2 * nb, KV, bs, hd), np.float32)
+    vp2 = np.zeros_like(kp2)
+    kp2[perm], vp2[perm] = kp1, vp1
+    lens = [150, 37]
+    t1 = np.stack([ident, ident]).astype(np.int32)
+    t2 = np.stack([perm, perm]).astype(np.int32)
+    a = oracle.attention_paged(q, kp1, vp1, t1, lens, 2, H, KV, hd, bs, nb, 0)
+    b = oracle.attention_paged(q, kp2, vp2, t2, lens, 2, H, KV, hd, bs, nb, 0)
+    assert np.array_equal(a, b)
+
+
+def test_paged_attention_window_equals_attention_over_the_last_rows():
+    rng = np.random.default_rng(23)
+    H, KV, hd, bs, nb = 4, 1, 64, 16, 8
+    C = bs * nb
+    q = rng.standard_normal(H * hd).astype(np.float32)
+    k = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    v = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    perm = np.arange(nb)
+    kp, vp = _pool_from_contiguous(k, bs, perm), _pool_from_contiguous(v, bs, perm)
+    T = 100
+    for W in (1, 7, 33, 99, 100, 500):
+        got = oracle.attention_paged(q, kp, vp, perm[None, :], [T], 1, H, KV, hd, bs, nb, W)
+        lo = max(0, T - W)
+        want = oracle.attention(q, np.ascontiguousarray(k[:, lo:T]), np.ascontiguousarray(v[:, lo:T]), H, KV, T - lo,
+                                T - lo, hd)
+        assert np.array_equal(got, want), W
