@@ -171,6 +171,37 @@ int ck_kv_store_bf16(void *k_cache, void *v_cache, const float *k, const float *
 int ck_kv_store_fp8(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
                     int cache_capacity, int head_dim, float k_scale, float v_scale, void *stream);
 
+/* Paged decode attention with an optional sliding window (page "paged decode
+ * attention": paged_decode_attn_bf16 / paged_decode_attn_fp8 and their GQA
+ * forms, arguments block_tables, seq_lens, max_blocks_per_seq, block_size,
+ * sliding_window, k_scale, v_scale), for a batch of sequences.
+ *   k_pool / v_pool: [num_blocks, num_kv_heads, block_size, head_dim]
+ *     elements of kv_dtype: 0 fp32, 1 bf16, 2 fp8 E4M3 (values as for
+ *     ck_attn_decode_gqa_bf16 / _fp8; k_scale / v_scale used for fp8 only);
+ *   block_tables: device int32 [batch, max_blocks_per_seq]: logical block i
+ *     of sequence b (its rows i*block_size ..) is physical block
+ *     block_tables[b][i];
+ *   seq_lens: device int32 [batch]: rows of sequence b, T_b;
+ *   q, out: fp32 [batch, num_heads * head_dim].
+ * Sequence b attends rows [T0, T_b) with T0 = max(0, T_b - sliding_window)
+ * when sliding_window > 0, else 0; out_b = the attention of
+ * ck_attn_decode_gqa over those rows.  On the device, T_b outside
+ * [0, max_blocks_per_seq * block_size] or a table entry outside
+ * [0, num_blocks) raises CK_ERANGE in the status word (the rows concerned are
+ * not read; a sequence with no rows attended gets zeros).
+ * Requirements: those of ck_attn_decode_gqa (bf16 / fp8: head_dim 64 or
+ * 128), 1 <= batch <= 1024, block_size >= 1, max_blocks_per_seq >= 1,
+ * num_blocks >= 1, sliding_window >= 0, every pointer 16-byte aligned.
+ * `scratch` >= ck_attn_paged_scratch_size(...) bytes with the same batch,
+ * heads, head_dim, block_size, max_blocks_per_seq and sliding_window. */
+size_t ck_attn_paged_scratch_size(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int sliding_window);
+int ck_attn_decode_gqa_paged(const float *q, const void *k_pool, const void *v_pool, float *out,
+                             const int32_t *block_tables, const int32_t *seq_lens, int batch, int num_heads,
+                             int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                             int sliding_window, int kv_dtype, float k_scale, float v_scale, void *scratch,
+                             size_t scratch_bytes, void *stream);
+
 /* ---- the whole layer step ---------------------------------------------- */
 
 /* mega_fused_attention_decode_q5_0 (page: MAIN KERNEL).  One token at

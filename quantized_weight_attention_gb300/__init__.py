@@ -26,7 +26,7 @@ __all__ = [
     "ck_block_dots_q5_0_q8_0", "ck_block_dots_q8_0_q8_0", "LIB_PATH", "ck_decode_layer_scratch_offset",
     "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8", "ck_attn_decode_gqa_noalloc",
     "CK_ATTN_NOALLOC_MAX_BYTES", "ck_attn_decode_gqa_bf16", "ck_attn_decode_gqa_fp8", "ck_kv_store_bf16",
-    "ck_kv_store_fp8",
+    "ck_kv_store_fp8", "ck_attn_paged_scratch_size", "ck_attn_decode_gqa_paged",
 ]
 
 CK_OK, CK_EINVAL, CK_ERANGE, CK_ESCRATCH, CK_EALIGN, CK_ECUDA, CK_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -58,6 +58,9 @@ _SIGS = {
     "ck_attn_decode_gqa_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _P, _SZ, _P]),
     "ck_kv_store_bf16": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "ck_kv_store_fp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _F, _F, _P]),
+    "ck_attn_paged_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "ck_attn_decode_gqa_paged": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _P, _SZ,
+                                      _P]),
     "ck_attn_decode_gqa_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "ck_decode_layer_scratch_size": (_SZ, [_I, _I, _I, _I, _I]),
     "ck_decode_layer": (_I, [_P] * 16 + [_I] * 6 + [_F, _P, _SZ, _P]),
@@ -177,6 +180,23 @@ def ck_kv_store_fp8(k_cache, v_cache, k, v, pos: int, num_kv_heads: int, cache_c
                     k_scale: float, v_scale: float, stream=None) -> int:
     return lib().ck_kv_store_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k), _ptr(v), pos, num_kv_heads, cache_capacity,
                                  head_dim, float(k_scale), float(v_scale), _stream(stream))
+
+
+def ck_attn_paged_scratch_size(batch: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                               max_blocks_per_seq: int, sliding_window: int) -> int:
+    return lib().ck_attn_paged_scratch_size(batch, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                            sliding_window)
+
+
+def ck_attn_decode_gqa_paged(q, k_pool, v_pool, out, block_tables, seq_lens, batch: int, num_heads: int,
+                             num_kv_heads: int, head_dim: int, block_size: int, max_blocks_per_seq: int,
+                             num_blocks: int, sliding_window: int, kv_dtype: int, k_scale: float, v_scale: float,
+                             scratch, scratch_bytes: int, stream=None) -> int:
+    """Paged decode attention with an optional sliding window (kv_dtype 0 fp32, 1 bf16, 2 fp8 E4M3)."""
+    return lib().ck_attn_decode_gqa_paged(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(out), _ptr(block_tables),
+                                          _ptr(seq_lens), batch, num_heads, num_kv_heads, head_dim, block_size,
+                                          max_blocks_per_seq, num_blocks, sliding_window, kv_dtype, float(k_scale),
+                                          float(v_scale), _ptr(scratch), scratch_bytes, _stream(stream))
 
 
 CK_ATTN_NOALLOC_MAX_BYTES = 2 * 1024 * 1024

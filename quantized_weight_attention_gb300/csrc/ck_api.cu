@@ -405,6 +405,68 @@ int ck_kv_store_fp8(void *k_cache, void *v_cache, const float *k, const float *v
                       stream);
 }
 
+// Paged attention: the rows a split plans for (the longest sequence the
+// tables can hold, or the window).
+static int paged_rows(int block_size, int max_blocks, int window) {
+    const long long cap = static_cast<long long>(block_size) * max_blocks;
+    const long long r = window > 0 && window < cap ? window : cap;
+    return r > (1 << 30) ? (1 << 30) : static_cast<int>(r);
+}
+
+size_t ck_attn_paged_scratch_size(int batch, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int sliding_window) {
+    if (batch < 1 || batch > 1024 || block_size < 1 || max_blocks_per_seq < 1 || sliding_window < 0) return 0;
+    if (attn_shape_ok(num_heads, num_kv_heads, head_dim)) return 0;
+    const int S = attn_splits_batched(batch, num_kv_heads, paged_rows(block_size, max_blocks_per_seq, sliding_window));
+    return attn_part_bytes(batch, num_heads, num_kv_heads, head_dim, S) + 256;
+}
+
+int ck_attn_decode_gqa_paged(const float *q, const void *k_pool, const void *v_pool, float *out,
+                             const int32_t *block_tables, const int32_t *seq_lens, int batch, int num_heads,
+                             int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                             int sliding_window, int kv_dtype, float k_scale, float v_scale, void *scratch,
+                             size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({q, k_pool, v_pool, out, block_tables, seq_lens}, {});
+    if (rc) return rc;
+    if ((rc = attn_shape_ok(num_heads, num_kv_heads, head_dim))) return rc;
+    if (batch < 1 || batch > 1024 || block_size < 1 || max_blocks_per_seq < 1 || num_blocks < 1 ||
+        sliding_window < 0)
+        return CK_EINVAL;
+    if (kv_dtype < 0 || kv_dtype > 2) return CK_EINVAL;
+    if (kv_dtype != 0 && head_dim != 64 && head_dim != 128) return CK_EINVAL;
+    if (kv_dtype == 2 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return CK_EINVAL;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    const int rows = paged_rows(block_size, max_blocks_per_seq, sliding_window);
+    const int S = attn_splits_batched(batch, num_kv_heads, rows);
+    if (scratch_bytes < attn_part_bytes(batch, num_heads, num_kv_heads, head_dim, S)) return CK_ESCRATCH;
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
+    AttnArgs a{};
+    a.q = q;
+    a.k_cache = static_cast<const float *>(k_pool);  // pools of kv_dtype elements
+    a.v_cache = static_cast<const float *>(v_pool);
+    a.kv_tokens = rows;  // the stage plan follows the longest split
+    a.H = num_heads;
+    a.KV = num_kv_heads;
+    a.hd = head_dim;
+    a.C = rows;
+    a.splits = S;
+    a.part = static_cast<float *>(scratch);
+    a.out = out;
+    a.kv_type = kv_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.window = sliding_window;
+    a.status = st;
+    return launch_attention(a, batch, as_stream(stream), false, false) ? CK_ECUDA : CK_OK;
+}
+
 static int attn_call(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
                      int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_type, float k_scale,
                      float v_scale, void *scratch, size_t scratch_bytes, void *stream) {

@@ -132,8 +132,9 @@ __device__ __forceinline__ float2 kv_load2(const uint8_t *p) {
 __host__ __device__ constexpr int at_prow(int G) { return 2 * ((G + 1) & ~1); }
 
 struct AttnSmem {
-    size_t off_full, off_empty, off_qbar, off_stage, off_q, off_p, off_alpha, off_ml, total;
+    size_t off_full, off_empty, off_qbar, off_stage, off_q, off_p, off_alpha, off_ml, off_bt, total;
 };
+constexpr int AT_BT_CACHE = 1024;  // block-table entries of a split held in shared memory (paged caches)
 
 __host__ __device__ inline AttnSmem attn_smem(int hd) {
     AttnSmem L;
@@ -154,6 +155,8 @@ __host__ __device__ inline AttnSmem attn_smem(int hd) {
     o += static_cast<size_t>(AT_CONSUMERS) * GMAX * 4;
     L.off_ml = o;
     o += static_cast<size_t>(2) * AT_CONSUMERS * GMAX * 4;
+    L.off_bt = o;
+    o += static_cast<size_t>(AT_BT_CACHE) * 4;
     L.total = (o + 127) / 128 * 128;
     return L;
 }
@@ -244,8 +247,15 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         }
     }
 
-    int T;
-    if (a.d_pos) {
+    int T, T0 = 0;  // rows [T0, T) are attended
+    if (a.block_tables) {  // paged cache: seq_lens[b] rows, the last `window` of them when window > 0
+        T = a.seq_lens[b];
+        if (T < 0 || T > a.max_blocks * a.block_size) {
+            if (s == 0 && g == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
+            T = 0;  // nothing attended: empty records
+        }
+        if (a.window > 0 && T > a.window) T0 = T - a.window;
+    } else if (a.d_pos) {
         const int pos = a.d_pos[b];
         if (pos < 0 || pos >= a.C) {
             if (s == 0 && g == 0 && threadIdx.x == 0) flag_error(a.status, FLAG_RANGE);
@@ -256,8 +266,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     } else {
         T = a.kv_tokens;
     }
-    const int chunk = a.chunk > 0 ? a.chunk : (T + S - 1) / S;
-    const int t0 = s * chunk;
+    const int chunk = a.chunk > 0 ? a.chunk : (T - T0 + S - 1) / S;
+    const int t0 = T0 + s * chunk;
     const int t1 = min(T, t0 + chunk);
     float *rec = a.part + ((static_cast<size_t>(b) * a.KV + g) * S + s) * part_stride(G, HD);
     if (t0 >= t1) {  // empty split: marked by m = -inf, skipped by the combine
@@ -269,10 +279,20 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
         }
         return;
     }
+    const bool paged = a.block_tables != nullptr;
     const uint8_t *kc = reinterpret_cast<const uint8_t *>(a.k_caches ? a.k_caches[b] : a.k_cache) +
-                        static_cast<size_t>(g) * a.C * HD * ES;
+                        (paged ? 0 : static_cast<size_t>(g) * a.C * HD * ES);
     const uint8_t *vc = reinterpret_cast<const uint8_t *>(a.v_caches ? a.v_caches[b] : a.v_cache) +
-                        static_cast<size_t>(g) * a.C * HD * ES;
+                        (paged ? 0 : static_cast<size_t>(g) * a.C * HD * ES);
+    // paged: this split's block-table entries (logical blocks lb0 ..) in shared memory
+    int *bts = reinterpret_cast<int *>(smem + L.off_bt);
+    const int bs = paged ? a.block_size : 1;
+    const int lb0 = paged ? t0 / bs : 0;
+    const int nbt = paged ? min((t1 - 1) / bs - lb0 + 1, AT_BT_CACHE) : 0;
+    if (paged && warp == 0) {
+        const int32_t *btr = a.block_tables + static_cast<size_t>(b) * a.max_blocks;
+        for (int i = lane; i < nbt; i += 32) bts[i] = btr[lb0 + i];
+    }
     const int ntiles = (t1 - t0 + AT_TILE - 1) / AT_TILE;
     constexpr int RS = at_rs(HD, BIG, ES), TPS = RS / AT_TILE, NSS = at_nss(HD, BIG, ES), LA = at_la(HD, BIG, ES);
 
@@ -305,10 +325,40 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
                 const int n = min(RS, t1 - r);
                 if (r + n >= T) pdl_wait();
                 uint8_t *dst = stage + static_cast<size_t>(sl) * 2 * RS * HD * ES;
-                const uint32_t bytes = static_cast<uint32_t>(n) * HD * ES;
-                mbar_arrive_expect_tx(&full[sl], 2 * bytes);
-                bulk_g2s(dst, kc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
-                bulk_g2s(dst + RS * HD * ES, vc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
+                if (!paged) {
+                    const uint32_t bytes = static_cast<uint32_t>(n) * HD * ES;
+                    mbar_arrive_expect_tx(&full[sl], 2 * bytes);
+                    bulk_g2s(dst, kc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
+                    bulk_g2s(dst + RS * HD * ES, vc + static_cast<size_t>(r) * HD * ES, bytes, &full[sl]);
+                } else {
+                    // rows r .. r + n - 1 as runs inside physical blocks
+                    // ([num_blocks][KV][block_size][hd]); an entry out of
+                    // range is flagged and its rows are not copied
+                    uint32_t total = 0;
+                    for (int u = r; u < r + n;) {
+                        const int lb = u / bs, o = u - lb * bs, m = min(r + n - u, bs - o);
+                        const int pb = lb - lb0 < AT_BT_CACHE ? bts[lb - lb0]
+                                                              : a.block_tables[static_cast<size_t>(b) * a.max_blocks + lb];
+                        if (pb >= 0 && pb < a.num_blocks) total += static_cast<uint32_t>(m) * HD * ES;
+                        u += m;
+                    }
+                    mbar_arrive_expect_tx(&full[sl], 2 * total);
+                    for (int u = r; u < r + n;) {
+                        const int lb = u / bs, o = u - lb * bs, m = min(r + n - u, bs - o);
+                        const int pb = lb - lb0 < AT_BT_CACHE ? bts[lb - lb0]
+                                                              : a.block_tables[static_cast<size_t>(b) * a.max_blocks + lb];
+                        if (pb >= 0 && pb < a.num_blocks) {
+                            const size_t src = ((static_cast<size_t>(pb) * a.KV + g) * bs + o) * HD * ES;
+                            const size_t off = static_cast<size_t>(u - r) * HD * ES;
+                            const uint32_t bytes = static_cast<uint32_t>(m) * HD * ES;
+                            bulk_g2s(dst + off, kc + src, bytes, &full[sl]);
+                            bulk_g2s(dst + RS * HD * ES + off, vc + src, bytes, &full[sl]);
+                        } else {
+                            flag_error(a.status, FLAG_RANGE);
+                        }
+                        u += m;
+                    }
+                }
             }
         }
         return;
@@ -643,7 +693,7 @@ __global__ void __launch_bounds__(256) k_attn_combine(const AttnArgs a) {
                 L = fmaf(sc, lred[w], L);
             }
         }
-        combine_store<HD>(a, b, h, blk, lane, __fdiv_rn(t, L));
+        combine_store<HD>(a, b, h, blk, lane, L > 0.0f ? __fdiv_rn(t, L) : 0.0f);  // no rows attended: 0
     }
 }
 
@@ -698,7 +748,7 @@ __global__ void __launch_bounds__(256) k_attn_combine_w(const AttnArgs a, int B)
             L = fmaf(sc, lv[s], L);
         }
     }
-    combine_store<HD>(a, b, h, blk, lane, __fdiv_rn(t, L));
+    combine_store<HD>(a, b, h, blk, lane, L > 0.0f ? __fdiv_rn(t, L) : 0.0f);  // no rows attended: 0
 }
 
 template <int DPL, int GT, int KT>

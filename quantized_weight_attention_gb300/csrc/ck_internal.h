@@ -130,6 +130,12 @@ struct AttnArgs {
     size_t l2_prefetch_bytes;
     int kv_type;              // cache elements: 0 fp32, 1 bf16, 2 fp8 E4M3 (k_cache / v_cache hold them)
     float k_scale, v_scale;   // fp8: k = code * k_scale, v = code * v_scale
+    // paged caches (block_tables non-null): k_cache / v_cache are pools
+    // [num_blocks][KV][block_size][hd]; sequence b attends rows [T0, T) with
+    // T = seq_lens[b], T0 = max(0, T - window) when window > 0; its logical
+    // block i is physical block block_tables[b * max_blocks + i]
+    const int32_t *block_tables, *seq_lens;
+    int block_size, max_blocks, num_blocks, window;
     unsigned *status;
 };
 size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
