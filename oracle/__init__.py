@@ -87,6 +87,7 @@ def lib():
             L.ref_kv_store.argtypes = [P, P, P, P, i, i, i, i]
             L.ref_attention.argtypes = [P, P, P, P, i, i, i, i, i]
             L.ref_decode_layer.argtypes = [P] * 16 + [i] * 6 + [f] + [P] * 6
+            L.ref_prefill_layer.argtypes = [P] * 16 + [i] * 7 + [f] + [P] * 6
             _lib = L
     return _lib
 
@@ -303,4 +304,30 @@ def decode_layer(x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_
                            _p(_u8(wo)), _p(_f32(gamma)), opt(bq), opt(bk), opt(bv), opt(bo), _p(k_cache),
                            _p(v_cache), _p(_f32(rope_cos)), _p(_f32(rope_sin)), pos, D, H, KV, hd, capacity,
                            float(eps), g("xq"), g("q"), g("k"), g("v"), g("attn"), g("aq"))
+    return (out, t) if taps else out
+
+
+def prefill_layer(x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos, rope_sin,
+                  pos: int, n: int, D: int, H: int, KV: int, hd: int, capacity: int, eps: float, taps: bool = False):
+    """The causal multi-token form: n tokens [n, D] at positions pos..pos+n-1.
+
+    k_cache / v_cache (float32, C-contiguous) get rows pos..pos+n-1 in place.
+    Returns ``out`` [n, D] or, with ``taps``, ``(out, dict_of_intermediates)``
+    whose entries are the decode layer's taps, one row per token.
+    """
+    assert k_cache.dtype == np.float32 and k_cache.flags.c_contiguous
+    assert v_cache.dtype == np.float32 and v_cache.flags.c_contiguous
+    assert 0 <= pos and pos + n <= capacity and n >= 1
+    out = np.empty((n, D), np.float32)
+    t = None
+    if taps:
+        t = dict(xq=np.empty((n, D // QK * Q8_0_BYTES), np.uint8), q=np.empty((n, H * hd), np.float32),
+                 k=np.empty((n, KV * hd), np.float32), v=np.empty((n, KV * hd), np.float32),
+                 attn=np.empty((n, H * hd), np.float32), aq=np.empty((n, H * hd // QK * Q8_0_BYTES), np.uint8))
+    g = (lambda nm: _p(t[nm])) if taps else (lambda nm: None)
+    opt = lambda a: None if a is None else _p(_f32(a))
+    lib().ref_prefill_layer(_p(out), _p(_f32(x)), _p(_f32(residual)), _p(_u8(wq)), _p(_u8(wk)), _p(_u8(wv)),
+                            _p(_u8(wo)), _p(_f32(gamma)), opt(bq), opt(bk), opt(bv), opt(bo), _p(k_cache),
+                            _p(v_cache), _p(_f32(rope_cos)), _p(_f32(rope_sin)), pos, n, D, H, KV, hd, capacity,
+                            float(eps), g("xq"), g("q"), g("k"), g("v"), g("attn"), g("aq"))
     return (out, t) if taps else out

@@ -627,3 +627,73 @@ void ref_decode_layer(float *out, const float *x, const float *residual, const u
     free(attn);
     free(xq);
 }
+
+/* ------------------------------------------------------------------------
+ * The multi-token (prefill) form of the same layer: n tokens of ONE sequence,
+ * token i at position pos + i, causal.  Page "C-Kernel-Engine" (kernel
+ * launchers), the prefill attention launcher: one query per (head, token)
+ * with a causal switch; read here as token i attending cache rows
+ * 0 .. pos + i, i.e. the rows already in the cache plus the chunk's own rows
+ * up to and including its own.
+ *
+ * The plain definition, in two phases: STEP 1 .. STEP 6 of the decode layer
+ * (norm, Q8_0 quant, projections, RoPE at pos + i, KV store at row pos + i)
+ * for every token, then STEP 7 .. STEP 8 (attention over pos + i + 1 rows,
+ * quant, O projection, residual) for every token.  x, residual, out:
+ * fp32 [n][D].  Taps as for ref_decode_layer, each [n][...] (NULL-able).
+ * ---------------------------------------------------------------------- */
+void ref_prefill_layer(float *out, const float *x, const float *residual, const uint8_t *wq, const uint8_t *wk,
+                       const uint8_t *wv, const uint8_t *wo, const float *gamma, const float *bq, const float *bk,
+                       const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                       const float *rope_sin, int pos, int n, int D, int H, int KV, int hd, int capacity, float eps,
+                       uint8_t *dbg_xq, float *dbg_q, float *dbg_k, float *dbg_v, float *dbg_attn, uint8_t *dbg_aq)
+{
+    const int QD = H * hd, KD = KV * hd;
+    const size_t xq_bytes = (size_t)(D / REF_QK) * REF_Q8_0_BYTES;
+    const size_t aq_bytes = (size_t)(QD / REF_QK) * REF_Q8_0_BYTES;
+    float *xn = (float *)malloc(sizeof(float) * (size_t)D);
+    float *q = (float *)malloc(sizeof(float) * (size_t)QD * (size_t)n);
+    float *k = (float *)malloc(sizeof(float) * (size_t)KD);
+    float *v = (float *)malloc(sizeof(float) * (size_t)KD);
+    float *attn = (float *)malloc(sizeof(float) * (size_t)QD);
+    uint8_t *xq = (uint8_t *)malloc(xq_bytes > aq_bytes ? xq_bytes : aq_bytes);
+
+    /* phase 1: every token's q, and its k / v stored at row pos + i */
+    for (int i = 0; i < n; ++i) {
+        float *qi = q + (size_t)i * QD;
+        ref_rmsnorm(x + (size_t)i * D, gamma, xn, D, eps);
+        ref_quantize_row_q8_0(xn, xq, D);
+        if (dbg_xq)
+            memcpy(dbg_xq + (size_t)i * xq_bytes, xq, xq_bytes);
+        ref_gemv(qi, wq, xq, bq, QD, D, 0);
+        ref_gemv(k, wk, xq, bk, KD, D, 0);
+        ref_gemv(v, wv, xq, bv, KD, D, 1);
+        ref_rope(qi, k, rope_cos, rope_sin, pos + i, H, KV, hd);
+        ref_kv_store(k_cache, v_cache, k, v, pos + i, KV, capacity, hd);
+        if (dbg_q)
+            memcpy(dbg_q + (size_t)i * QD, qi, sizeof(float) * (size_t)QD);
+        if (dbg_k)
+            memcpy(dbg_k + (size_t)i * KD, k, sizeof(float) * (size_t)KD);
+        if (dbg_v)
+            memcpy(dbg_v + (size_t)i * KD, v, sizeof(float) * (size_t)KD);
+    }
+    /* phase 2: causal attention, then the O projection and the residual */
+    for (int i = 0; i < n; ++i) {
+        float *oi = out + (size_t)i * D;
+        ref_attention(q + (size_t)i * QD, k_cache, v_cache, attn, H, KV, pos + i + 1, capacity, hd);
+        if (dbg_attn)
+            memcpy(dbg_attn + (size_t)i * QD, attn, sizeof(float) * (size_t)QD);
+        ref_quantize_row_q8_0(attn, xq, QD);
+        if (dbg_aq)
+            memcpy(dbg_aq + (size_t)i * aq_bytes, xq, aq_bytes);
+        ref_gemv(oi, wo, xq, bo, D, QD, 0);
+        for (int e = 0; e < D; ++e)
+            oi[e] = oi[e] + residual[(size_t)i * D + e];
+    }
+    free(xn);
+    free(q);
+    free(k);
+    free(v);
+    free(attn);
+    free(xq);
+}
