@@ -46,9 +46,11 @@ def parse():
     p.add_argument("--warmup", type=int, default=600)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="7b8k",
-                   choices=["tiny", "small1k", "7b8k", "stack32k", "batched64", "attn32k"])
+                   choices=["tiny", "small1k", "7b8k", "stack32k", "batched64", "attn32k", "paged64", "prefill512"])
     p.add_argument("--kv-dtype", default="bf16", choices=["f32", "bf16", "fp8"],
-                   help="attn32k: cache element type (fp8 = E4M3 with per-tensor scales)")
+                   help="attn32k / paged64: cache element type (fp8 = E4M3 with per-tensor scales)")
+    p.add_argument("--window", type=int, default=0, help="paged64: sliding window (0: every row)")
+    p.add_argument("--block-size", type=int, default=64, help="paged64: rows per cache block")
     p.add_argument("--layers", type=int, default=0, help="stack32k: layers in the stack (default: all 28)")
     p.add_argument("--kv-cap", type=int, default=0,
                    help="batched64: cap every cache at this many rows (a small case for profilers; not the workload)")
@@ -219,6 +221,10 @@ def run_ours(args, ws, rank, local, pg):
     torch.cuda.set_device(dev)
     if args.config == "attn32k":
         return run_attn_kv(args, ws, pg, torch, q, synth, dev)
+    if args.config == "paged64":
+        return run_paged(args, ws, pg, torch, q, synth, dev)
+    if args.config == "prefill512":
+        return run_prefill(args, ws, pg, torch, q, synth, dev)
     w = synth.WORKLOADS[args.config]
     if args.config == "stack32k":
         return run_stack(args, ws, pg, torch, q, synth, dev)
@@ -593,6 +599,311 @@ def cpu_baseline_attn(synth, dt, budget_s):
                       f"{el:.1f} s, cpu: {cpu_model()}"}
 
 
+def paged_plan(synth, bs):
+    """The batched64 sequences (lengths from its seed) in a pool of bs-row
+    blocks placed in a shuffled order: tables [B, max_blocks], lengths [B]."""
+    w = synth.WORKLOADS["batched64"]
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    lens = synth.batched_lengths(w, rng).astype(np.int32)
+    maxb = -(-int(w.kv_hi + 1) // bs)
+    need = [-(-int(n) // bs) for n in lens]
+    nblk = int(sum(need))
+    order = np.random.Generator(np.random.PCG64(w.seed + 1)).permutation(nblk).astype(np.int32)
+    tables = np.zeros((w.batch, maxb), np.int32)
+    o = 0
+    for b, k in enumerate(need):
+        tables[b, :k] = order[o:o + k]
+        o += k
+    return w, lens, tables, maxb, nblk
+
+
+def run_paged(args, ws, pg, torch, q, synth, dev):
+    """Paged decode attention for the 64 batched64 sequences: one C-ABI call
+    per step (a token for every sequence), the pool holding exactly their rows
+    in shuffled blocks."""
+    bs, dt, win = args.block_size, args.kv_dtype, args.window
+    w, lens, tables, maxb, nblk = paged_plan(synth, bs)
+    B, H, KV, hd = w.batch, w.H, w.KV, w.hd
+    es = KV_ES[dt]
+    kind = {"f32": 0, "bf16": 1, "fp8": 2}[dt]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    shape = (nblk, KV, bs, hd)
+    if dt == "fp8":
+        mk = lambda: (torch.randint(0, 0x7F, shape, generator=gen, device=dev, dtype=torch.int32) |
+                      (torch.randint(0, 2, shape, generator=gen, device=dev, dtype=torch.int32) << 7)).to(torch.uint8)
+    else:
+        f = torch.float32 if dt == "f32" else torch.bfloat16
+        mk = lambda: torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(f)
+    kp, vp = mk(), mk()
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    td, ld = T(tables), T(lens)
+    qv = torch.randn(B * H * hd, generator=gen, device=dev, dtype=torch.float32)
+    out = torch.empty(B * H * hd, dtype=torch.float32, device=dev)
+    nbytes = q.ck_attn_paged_scratch_size(B, H, KV, hd, bs, maxb, win)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    ks = vs = 0.01
+
+    def call(qin=None):
+        return q.ck_attn_decode_gqa_paged(qv if qin is None else qin, kp, vp, out, td, ld, B, H, KV, hd, bs, maxb,
+                                          nblk, win, kind, ks, vs, scratch, nbytes, stream.cuda_stream)
+
+    with torch.cuda.stream(stream):
+        q.check(call())
+    torch.cuda.synchronize()
+    n_g = 10
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n_g):
+            q.check(call())
+    K = min(max(1, -(-args.steps // n_g)) * n_g, 400)
+    W = max(args.warmup, 3)
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // n_g)):
+            g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // n_g):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    rows = int(sum(min(int(n), win) if win > 0 else int(n) for n in lens))
+    kv_bytes = rows * KV * hd * es * 2
+    ach = kv_bytes * ws * K / sec / 1e9
+    peak, peak_kind = measured_peaks()
+    Ke = min(K, 200)
+    qh = qv.cpu().pin_memory()
+    oh = torch.empty(B * H * hd, dtype=torch.float32).pin_memory()
+    qd = torch.empty_like(qv)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(Ke):
+            qd.copy_(qh, non_blocking=True)
+            q.check(call(qd))
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1))
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    line = {"metric": "paged decode attention tokens/s and achieved HBM GB/s vs GB300 peak",
+            "value": round(ws * B * K / sec, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f32": "f32", "bf16": "bf16 cache, f32 math", "fp8": "fp8 e4m3 cache, f32 math"}[dt],
+            "data": "synthetic",
+            "config": {"workload": f"paged64: the 64 batched64 sequences (lengths uniform in [{w.kv_lo}, {w.kv_hi}], "
+                                   f"sum {int(sum(lens))}) in a pool of {nblk} blocks of {bs} rows ({dt}), "
+                                   f"shuffled; window {win or 'none'} ({rows} rows attended); one call per step",
+                       "l2": f"{kv_bytes / 1e9:.2f} GB per step >> L2"},
+            "step_hbm_gbs": round(ach, 1), "step_bytes": kv_bytes,
+            "roofline": {"kernel": "paged attention (split + combine, one call)", "bound": "hbm",
+                         "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                         "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None},
+            "e2e": {"value": round(ws * B * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": B * H * hd * 4, "d2h_bytes_per_step": B * H * hd * 4, "steps": Ke,
+                    "how": "per call: pinned q [B, H*hd] -> device, the paged attention call, out -> pinned host"},
+            "gpu_launches": 2 * K, "clocks": clocks}
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        line["cpu_baseline"] = cpu_baseline_paged(synth, dt, bs, win, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_paged(synth, dt, bs, win, budget_s):
+    """The oracle paged attention sequence by sequence (the same lengths and
+    block size) until the budget: tokens/s over the sequences done."""
+    import oracle
+    oracle.lib()
+    w, lens, tables, maxb, nblk = paged_plan(synth, bs)
+    H, KV, hd = w.H, w.KV, w.hd
+    kind = {"f32": 0, "bf16": 1, "fp8": 2}[dt]
+    rng = np.random.default_rng(9)
+    done, el = 0, 0.0
+    for b in range(w.batch):
+        need = -(-int(lens[b]) // bs)
+        if dt == "fp8":
+            kp = (rng.integers(0, 0x7F, (need, KV, bs, hd)) | (rng.integers(0, 2, (need, KV, bs, hd)) << 7)
+                  ).astype(np.uint8)
+        else:
+            kf = rng.standard_normal((need, KV, bs, hd)).astype(np.float32)
+            kp = oracle.bf16_from_f32(kf) if dt == "bf16" else kf
+        qv = rng.standard_normal(H * hd).astype(np.float32)
+        tbl = np.arange(need, dtype=np.int32)[None, :]
+        t0 = time.perf_counter()
+        oracle.attention_paged(qv, kp, kp, tbl, [int(lens[b])], 1, H, KV, hd, bs, need, win, kind, 0.01, 0.01)
+        el += time.perf_counter() - t0
+        done += 1
+        if el >= budget_s:
+            break
+    return {"value": round(done / el, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of the 64 sequences (paged, {dt}, block {bs}, window {win or 'none'}) by the "
+                      f"single-threaded C oracle, {el:.1f} s, cpu: {cpu_model()}"}
+
+
+PREFILL_POS, PREFILL_N = 7680, 512  # the last 512-token chunk of an 8192-token prompt
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # fp32 FMA lanes x 2 flops x max SM clock
+
+
+def prefill_workload(synth):
+    return dataclasses.replace(synth.WORKLOADS["7b8k"], pos=PREFILL_POS)
+
+
+def prefill_attn_flops(pos, n, H, hd):
+    """QK and PV, 2 flops per multiply-add each: token i sees pos + i + 1 rows."""
+    rows = n * pos + n * (n + 1) // 2
+    return 4 * rows * H * hd
+
+
+def run_prefill(args, ws, pg, torch, q, synth, dev):
+    """The 7B-shaped layer prefilling tokens 7680..8191 of a prompt in one
+    ck_prefill_layer call per step (512 tokens, causal over the cache);
+    replicas of weights and caches rotate to keep the working set over L2."""
+    w = prefill_workload(synth)
+    P, n = PREFILL_POS, PREFILL_N
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
+    x0 = rng.standard_normal((n, w.D)).astype(np.float32)
+    cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+    per_rep = w.weight_bytes() + 2 * w.KV * w.capacity * w.hd * 4
+    R = max(1, -(-3 * l2 // per_rep))
+    gen = torch.Generator(device=dev)
+    reps = []
+    for r in range(R):
+        g = dict(gamma=T(gamma), wq=T(wq), wk=T(wk), wv=T(wv), wo=T(wo), bq=T(bq), bk=T(bk), bv=T(bv), bo=T(bo))
+        gen.manual_seed(w.seed * 100 + r)
+        g["kc"] = torch.zeros((w.KV, w.capacity, w.hd), dtype=torch.float32, device=dev)
+        g["vc"] = torch.zeros_like(g["kc"])
+        g["kc"][:, :P].normal_(generator=gen)
+        g["vc"][:, :P].normal_(generator=gen)
+        reps.append(g)
+    cosd, sind = T(cos), T(sin)
+    xd = T(x0)
+    out = torch.empty((n, w.D), dtype=torch.float32, device=dev)
+    nbytes = q.ck_prefill_layer_scratch_size(n, w.D, w.H, w.KV, w.hd, w.capacity)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(g, xin):
+        q.check(q.ck_prefill_layer(out, xin, xin, g["wq"], g["wk"], g["wv"], g["wo"], g["gamma"], g["bq"], g["bk"],
+                                   g["bv"], g["bo"], g["kc"], g["vc"], cosd, sind, P, n, w.D, w.H, w.KV, w.hd,
+                                   w.capacity, w.eps, scratch, nbytes, stream.cuda_stream))
+
+    with torch.cuda.stream(stream):
+        step(reps[0], xd)
+    torch.cuda.synchronize()
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for g in reps:
+            step(g, xd)
+    K = max(1, -(-min(args.steps, 400) // R)) * R
+    W = max(args.warmup, 3)
+    with torch.cuda.stream(stream):
+        for _ in range(-(-W // R)):
+            graph.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(pg, torch)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(K // R):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    barrier(pg, torch)
+    clocks = sampler.stop()
+    ms = max_over_ranks(pg, torch, ev0.elapsed_time(ev1))
+    sec = ms / 1e3
+    fl = prefill_attn_flops(P, n, w.H, w.hd)
+    ach = fl * K / sec / 1e12
+
+    # e2e: the chunk's rows from pinned host memory, its output rows back
+    Ke = min(K, 50)
+    xh = torch.from_numpy(x0).pin_memory()
+    oh = torch.empty((n, w.D), dtype=torch.float32).pin_memory()
+    xe = torch.empty((n, w.D), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(Ke):
+            xe.copy_(xh, non_blocking=True)
+            step(reps[i % R], xe)
+            oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+    e1.synchronize()
+    e2e_ms = max_over_ranks(pg, torch, e0.elapsed_time(e1))
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0, (rc, st)
+    line = {"metric": "prefill tokens/s of the layer (causal chunk over the cache)",
+            "value": round(ws * n * K / sec, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8/int5 codes: exact integer block dots (tcgen05 f16); fp32 attention", "data": "synthetic",
+            "config": {"workload": f"prefill512: the D=3584 28/4-head hd=128 layer, tokens {P}..{P + n - 1} of one "
+                                   f"sequence in one ck_prefill_layer call per step (causal: token i attends "
+                                   f"{P} + i + 1 rows)",
+                       "l2": f"{R} replicas of weights + caches ({per_rep / 1e6:.0f} MB each) in rotation"},
+            "attn_flops_per_step": fl,
+            "roofline": {"kernel": "whole prefill step (attention flops)", "bound": "alu",
+                         "achieved": round(ach, 2), "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
+                         "peak_kind": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz", "traffic": None},
+            "e2e": {"value": round(ws * n * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": n * w.D * 4, "d2h_bytes_per_step": n * w.D * 4, "steps": Ke,
+                    "how": "per step: pinned x [n, D] -> device, ck_prefill_layer, out -> pinned host"},
+            "gpu_launches": 6 * K, "clocks": clocks}
+    if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
+        line["cpu_baseline"] = cpu_baseline_prefill(synth, args.cpu_seconds)
+    return line
+
+
+def cpu_baseline_prefill(synth, budget_s):
+    """The oracle's prefill form on the first m tokens of the chunk (m sized
+    from a 4-token probe to fill about budget_s): tokens/s."""
+    import oracle
+    oracle.lib()
+    w = prefill_workload(synth)
+    P = PREFILL_POS
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    gamma, wq, wk, wv, wo, bq, bk, bv, bo = synth.draw_weights(rng, w)
+    x0 = rng.standard_normal((PREFILL_N, w.D)).astype(np.float32)
+    kc, vc = synth.draw_cache(rng, w, P)
+    cos, sin = synth.rope_tables(w.capacity, w.hd, w.theta)
+
+    def run(m):
+        k2, v2 = kc.copy(), vc.copy()
+        t0 = time.perf_counter()
+        oracle.prefill_layer(x0[:m], x0[:m], wq, wk, wv, wo, gamma, bq, bk, bv, bo, k2, v2, cos, sin, P, m, w.D, w.H,
+                             w.KV, w.hd, w.capacity, w.eps)
+        return time.perf_counter() - t0
+
+    t4 = run(4)
+    m = int(min(PREFILL_N, max(4, budget_s / max(t4 / 4, 1e-6))))
+    el = run(m)
+    return {"value": round(m / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"tokens {P}..{P + m - 1} ({m} of the 512) by the single-threaded C oracle's prefill form, "
+                      f"{el:.1f} s, cpu: {cpu_model()}"}
+
+
 def run_batched(args, ws, pg, torch, q, synth, dev):
     """64 sequences of the 7B-shaped layer with ragged caches (lengths uniform
     in [512, 16384]): one ck_decode_layer_batched call per step."""
@@ -776,6 +1087,24 @@ def cpu_baseline(w, budget_s):
 
 def run_reference(args, ws):
     from quantized_weight_attention_gb300 import synth
+    if args.config == "prefill512":  # the oracle prefill form, as the CPU baseline
+        cb = cpu_baseline_prefill(synth, 30.0)
+        return {"impl": "reference", "metric": "prefill tokens/s of the layer (causal chunk over the cache)",
+                "value": cb["value"], "unit": "tokens/s", "n_gpus": ws, "steps": 1, "warmup": 0,
+                "ms_per_step": round(1e3 * PREFILL_N / cb["value"], 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64 accumulation (C oracle)", "data": "synthetic",
+                "config": {"workload": "prefill512 (same as the GPU arm)"},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
+    if args.config == "paged64":  # the oracle paged attention, as the CPU baseline
+        cb = cpu_baseline_paged(synth, args.kv_dtype, args.block_size, args.window, 60.0)
+        return {"impl": "reference", "metric": "paged decode attention tokens/s and achieved HBM GB/s vs GB300 peak",
+                "value": cb["value"], "unit": "tokens/s", "n_gpus": ws, "steps": 1, "warmup": 0,
+                "ms_per_step": round(1e3 * 64 / cb["value"], 3), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64 accumulation (C oracle)", "data": "synthetic",
+                "config": {"workload": f"paged64, {args.kv_dtype} cache (same as the GPU arm)"},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
     if args.config == "attn32k":  # the oracle attention, as the CPU baseline
         cb = cpu_baseline_attn(synth, args.kv_dtype, 60.0)
         return {"impl": "reference", "metric": "decode attention calls/s and achieved HBM GB/s vs GB300 peak",

@@ -297,6 +297,36 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
 size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim, int num_heads, int num_kv_heads,
                                               int head_dim, int cache_capacity);
 
+/* ---- the multi-token (prefill) form of the layer ------------------------ */
+
+/* Page "C-Kernel-Engine" (kernel launchers): the prefill attention launcher,
+ * one query per (head, token) with a causal switch.  Read here as the same
+ * layer applied to `n_tokens` consecutive tokens of ONE sequence: token i sits
+ * at position pos + i, its K / V rows are stored at row pos + i, and it
+ * attends cache rows 0 .. pos + i (the rows already in the cache and the
+ * chunk's own rows up to and including its own).  The result equals
+ * n_tokens calls of ck_decode_layer at positions pos, pos + 1, ... in order.
+ * out, x, residual: fp32 [n_tokens, embed_dim] (device; out must not alias x
+ * or residual; residual may alias x).  k_cache, v_cache: head-major fp32
+ * [num_kv_heads, cache_capacity, head_dim] (device, 16-byte aligned, else
+ * CK_EALIGN); rows pos .. pos + n_tokens - 1 are written.  Weights, biases,
+ * gamma, rope tables and eps as for ck_decode_layer.  Requirements: 1 <=
+ * n_tokens <= 1024 and the shape requirements of ck_decode_layer_batched,
+ * otherwise CK_EINVAL; pos >= 0 and pos + n_tokens <= cache_capacity,
+ * otherwise CK_ERANGE (checked on the host, nothing launched).
+ * `scratch`: >= ck_prefill_layer_scratch_size(...) bytes of device memory
+ * (no initialization needed); the taps (CK_TAP_*) sit at
+ * ck_prefill_layer_scratch_offset(...), row i for token i. */
+size_t ck_prefill_layer_scratch_size(int n_tokens, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                     int cache_capacity);
+size_t ck_prefill_layer_scratch_offset(int tap, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
+                                       int head_dim, int cache_capacity);
+int ck_prefill_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                     const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                     const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                     const float *rope_sin, int pos, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
+                     int head_dim, int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream);
+
 /* ---- test access to the integer block dots ----------------------------- */
 
 /* The per-block int32 dots that the GEMVs above compute, with the same

@@ -22,6 +22,7 @@ __all__ = [
     "CK_OK", "CK_EINVAL", "CK_ERANGE", "CK_ESCRATCH", "CK_EALIGN", "CK_ECUDA", "CK_ETIMEOUT", "CkError",
     "lib", "check", "ck_status_string", "ck_quantize_q8_0", "ck_gemv_q5_0_q8_0", "ck_gemv_q8_0_q8_0",
     "ck_rope_inplace", "ck_kv_store", "ck_attn_scratch_size", "ck_attn_decode_gqa",
+    "ck_prefill_layer_scratch_size", "ck_prefill_layer_scratch_offset", "ck_prefill_layer",
     "ck_decode_layer_scratch_size", "ck_decode_layer", "ck_decode_layer_devpos", "ck_device_status",
     "ck_block_dots_q5_0_q8_0", "ck_block_dots_q8_0_q8_0", "LIB_PATH", "ck_decode_layer_scratch_offset",
     "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8", "ck_attn_decode_gqa_noalloc",
@@ -70,6 +71,9 @@ _SIGS = {
     "ck_decode_layer_batched_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "ck_decode_layer_batched": (_I, [_P] * 17 + [_I] * 6 + [_F, _P, _SZ, _P]),
     "ck_decode_layer_batched_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "ck_prefill_layer_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "ck_prefill_layer_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    "ck_prefill_layer": (_I, [_P] * 16 + [_I] * 7 + [_F, _P, _SZ, _P]),
     "ck_block_dots_q5_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
     "ck_block_dots_q8_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
 }
@@ -271,6 +275,28 @@ def ck_decode_layer_batched_scratch_offset(tap: int, batch: int, embed_dim: int,
                                            head_dim: int, cache_capacity: int) -> int:
     return lib().ck_decode_layer_batched_scratch_offset(tap, batch, embed_dim, num_heads, num_kv_heads, head_dim,
                                                         cache_capacity)
+
+
+def ck_prefill_layer_scratch_size(n_tokens: int, embed_dim: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                  cache_capacity: int) -> int:
+    return lib().ck_prefill_layer_scratch_size(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim,
+                                               cache_capacity)
+
+
+def ck_prefill_layer_scratch_offset(tap: int, n_tokens: int, embed_dim: int, num_heads: int, num_kv_heads: int,
+                                    head_dim: int, cache_capacity: int) -> int:
+    return lib().ck_prefill_layer_scratch_offset(tap, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim,
+                                                 cache_capacity)
+
+
+def ck_prefill_layer(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos, rope_sin,
+                     pos: int, n_tokens: int, embed_dim: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                     cache_capacity: int, eps: float, scratch, scratch_bytes: int, stream=None) -> int:
+    """n_tokens consecutive tokens of one sequence at positions pos.. (causal); x / out [n_tokens, embed_dim]."""
+    return lib().ck_prefill_layer(
+        _ptr(out), _ptr(x), _ptr(residual), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _ptr(gamma), _ptr(bq), _ptr(bk),
+        _ptr(bv), _ptr(bo), _ptr(k_cache), _ptr(v_cache), _ptr(rope_cos), _ptr(rope_sin), pos, n_tokens, embed_dim,
+        num_heads, num_kv_heads, head_dim, cache_capacity, eps, _ptr(scratch), scratch_bytes, _stream(stream))
 
 
 def ck_block_dots_q5_0_q8_0(isum, W, x_q8, M: int, K: int, stream=None) -> int:

@@ -551,23 +551,15 @@ size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim,
     }
 }
 
-int ck_decode_layer_batched(float *out, const float *x, const float *residual, const void *wq, const void *wk,
-                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
-                            const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
-                            const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch,
-                            int embed_dim, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
-                            float eps, void *scratch, size_t scratch_bytes, void *stream) {
-    int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_caches, v_caches, rope_cos, rope_sin, d_pos},
-                        {bq, bk, bv, bo});
-    if (rc) return rc;
-    if ((rc = batch_shape_check(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))) return rc;
-    if (!scratch) return CK_ESCRATCH;
-    if (!aligned16(scratch)) return CK_EALIGN;
-    const BatchScratch L = batch_scratch(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
-    if (scratch_bytes < L.total) return CK_ESCRATCH;
-    if (out == x || out == residual) return CK_EINVAL;
-    uint8_t *sc = static_cast<uint8_t *>(scratch);
-    cudaStream_t s = as_stream(stream);
+// The launches of a batched step on validated arguments: norm + pack, the Q/K/V
+// projections (with RoPE and the KV stores), attention, the O projection.
+// pdl_first: whether the first launch may overlap the stream's preceding work.
+static int batched_body(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                        const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                        const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
+                        const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch, int embed_dim,
+                        int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps, uint8_t *sc,
+                        const BatchScratch &L, cudaStream_t s, bool pdl_first, int chunk_pos) {
     unsigned *st = status_word();
     if (!st) return CK_ECUDA;
 
@@ -612,7 +604,7 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
         ba.tickets_o = L.tp.tickets_o;
         ba.n_tickets = L.tp.tickets;
     }
-    if (launch_norm_pack(ba, s, true)) return CK_ECUDA;
+    if (launch_norm_pack(ba, s, pdl_first)) return CK_ECUDA;
     if ((tc ? launch_rows_tc(ba, false, s, true) : launch_rows_batched(ba, false, s, true))) return CK_ECUDA;
 
     AttnArgs aa{};
@@ -631,12 +623,98 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
     aa.out_pack = ba.apack;
     aa.out_img = ba.aimg;
     aa.img_groups = img_groups(batch);
+    if (chunk_pos >= 0) {  // prefill: every row from the chunk's start is new
+        aa.fresh_chunk = 1;
+        aa.fresh_from = chunk_pos;
+    }
     aa.l2_prefetch = wo;
     aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
     aa.status = st;
     if (launch_attention(aa, batch, s, true, true)) return CK_ECUDA;
     if ((tc ? launch_rows_tc(ba, true, s, true) : launch_rows_batched(ba, true, s, true))) return CK_ECUDA;
     return CK_OK;
+}
+
+int ck_decode_layer_batched(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                            const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
+                            const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch,
+                            int embed_dim, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
+                            float eps, void *scratch, size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_caches, v_caches, rope_cos, rope_sin, d_pos},
+                        {bq, bk, bv, bo});
+    if (rc) return rc;
+    if ((rc = batch_shape_check(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))) return rc;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    const BatchScratch L = batch_scratch(batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
+    if (scratch_bytes < L.total) return CK_ESCRATCH;
+    if (out == x || out == residual) return CK_EINVAL;
+    return batched_body(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_caches, v_caches, rope_cos,
+                        rope_sin, d_pos, batch, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps,
+                        static_cast<uint8_t *>(scratch), L, as_stream(stream), true, -1);
+}
+
+// ---- the multi-token (prefill) form ----------------------------------------
+// The chunk's n tokens run as a batch of n entries over the one cache; the
+// per-entry cache pointers and positions live after the batched scratch.
+struct PrefillScratch {
+    BatchScratch b;
+    size_t off_kcs, off_vcs, off_pos, total;
+};
+
+static PrefillScratch prefill_scratch(int n, int D, int H, int KV, int hd, int C) {
+    PrefillScratch P{};
+    P.b = batch_scratch(n, D, H, KV, hd, C);
+    size_t o = P.b.total;
+    P.off_kcs = o;
+    o = a256(o + static_cast<size_t>(n) * sizeof(float *));
+    P.off_vcs = o;
+    o = a256(o + static_cast<size_t>(n) * sizeof(float *));
+    P.off_pos = o;
+    o = a256(o + static_cast<size_t>(n) * 4);
+    P.total = o;
+    return P;
+}
+
+size_t ck_prefill_layer_scratch_size(int n_tokens, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
+                                     int cache_capacity) {
+    if (batch_shape_check(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity)) return 0;
+    return prefill_scratch(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity).total;
+}
+
+size_t ck_prefill_layer_scratch_offset(int tap, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
+                                       int head_dim, int cache_capacity) {
+    return ck_decode_layer_batched_scratch_offset(tap, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim,
+                                                  cache_capacity);
+}
+
+int ck_prefill_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                     const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                     const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                     const float *rope_sin, int pos, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
+                     int head_dim, int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_cache, v_cache, rope_cos, rope_sin},
+                        {bq, bk, bv, bo});
+    if (rc) return rc;
+    if ((rc = batch_shape_check(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))) return rc;
+    if (pos < 0 || pos > cache_capacity - n_tokens) return CK_ERANGE;
+    if (!aligned16(k_cache) || !aligned16(v_cache)) return CK_EALIGN;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    const PrefillScratch P = prefill_scratch(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity);
+    if (scratch_bytes < P.total) return CK_ESCRATCH;
+    if (out == x || out == residual) return CK_EINVAL;
+    uint8_t *sc = static_cast<uint8_t *>(scratch);
+    cudaStream_t s = as_stream(stream);
+    float **kcs = reinterpret_cast<float **>(sc + P.off_kcs);
+    float **vcs = reinterpret_cast<float **>(sc + P.off_vcs);
+    int32_t *pos_of = reinterpret_cast<int32_t *>(sc + P.off_pos);
+    if (launch_prefill_setup(kcs, vcs, pos_of, k_cache, v_cache, pos, n_tokens, s)) return CK_ECUDA;
+    // the first batched launch waits for the whole setup grid (no overlap)
+    return batched_body(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, kcs, vcs, rope_cos, rope_sin,
+                        pos_of, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps, sc,
+                        P.b, s, false, pos);
 }
 
 size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,

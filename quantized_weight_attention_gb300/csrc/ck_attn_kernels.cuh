@@ -306,11 +306,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
     pdl_trigger();
 
     if (warp == 0) {
-        // ---- producer.  Rows before T-1 are never written by the preceding
-        // grid, so they stream before waiting on it; the super-stage holding
-        // row T-1 (the row just stored) waits first.  Super-stage k is issued
-        // once super-stage k - LA has arrived and its slot is free.
+        // ---- producer.  Rows before `fresh` are never written by the
+        // preceding grid, so they stream before waiting on it; a super-stage
+        // holding a row from `fresh` on (the row just stored, or a prefill
+        // chunk's rows) waits first.  Super-stage k is issued once
+        // super-stage k - LA has arrived and its slot is free.
         if (lane == 0) {
+            const int fresh = a.fresh_chunk ? min(a.fresh_from, T - 1) : T - 1;
             const int nss = (t1 - t0 + RS - 1) / RS;
             for (int k = 0; k < nss; ++k) {
                 const int sl = k % NSS;
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) k_attn_split(const AttnArgs a) 
                 }
                 const int r = t0 + k * RS;
                 const int n = min(RS, t1 - r);
-                if (r + n >= T) pdl_wait();
+                if (r + n > fresh) pdl_wait();
                 uint8_t *dst = stage + static_cast<size_t>(sl) * 2 * RS * HD * ES;
                 if (!paged) {
                     const uint32_t bytes = static_cast<uint32_t>(n) * HD * ES;

@@ -226,6 +226,27 @@ bool batched_shape_ok(int D, int H, int hd) {
     return D % 256 == 0 && nb <= 128 && nbo % 8 == 0 && nbo <= 128;
 }
 
+// The multi-token (prefill) form runs as a batch whose entries are the chunk's
+// tokens: every entry names the one cache, entry i sits at position pos + i.
+__global__ void k_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos,
+                                int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        kcs[i] = k_cache;
+        vcs[i] = v_cache;
+        pos_of[i] = pos + i;
+    }
+}
+
+int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos, int n,
+                         cudaStream_t s) {
+    void *args[] = {&kcs, &vcs, &pos_of, &k_cache, &v_cache, &pos, &n};
+    return launch(reinterpret_cast<const void *>(k_prefill_setup), dim3((n + 255) / 256), dim3(256), 0, s, false,
+                  args) == cudaSuccess
+               ? 0
+               : -5;
+}
+
 int launch_norm_pack(const BatchArgs &a0, cudaStream_t s, bool pdl) {
     BatchArgs a = a0;
     const size_t smem = xpack_bytes(a.D / QK);

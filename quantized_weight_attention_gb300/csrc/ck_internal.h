@@ -102,6 +102,8 @@ struct TpPlan {
 TpPlan tp_plan(int B, int D, int H, int KV, int hd, bool with_device);
 int launch_rows_tc(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 int launch_norm_pack(const BatchArgs &a, cudaStream_t s, bool pdl);
+int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos, int n,
+                         cudaStream_t s);
 int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);
 
@@ -136,6 +138,9 @@ struct AttnArgs {
     // block i is physical block block_tables[b * max_blocks + i]
     const int32_t *block_tables, *seq_lens;
     int block_size, max_blocks, num_blocks, window;
+    // cache rows the preceding grid may have written: row T - 1 alone when
+    // fresh_chunk is 0; rows fresh_from .. T - 1 otherwise (a prefill chunk)
+    int fresh_chunk, fresh_from;
     unsigned *status;
 };
 size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
