@@ -50,6 +50,9 @@ def parse():
     p.add_argument("--kv-dtype", default="bf16", choices=["f32", "bf16", "fp8"],
                    help="attn32k / paged64: cache element type (fp8 = E4M3 with per-tensor scales)")
     p.add_argument("--window", type=int, default=0, help="paged64: sliding window (0: every row)")
+    p.add_argument("--rows", type=int, default=0, help="attn32k: rows attended (default 32769)")
+    p.add_argument("--splits", type=int, default=-1,
+                   help="attn32k: split count through ck_attn_decode_gqa_split (0: its built-in choice)")
     p.add_argument("--block-size", type=int, default=64, help="paged64: rows per cache block")
     p.add_argument("--layers", type=int, default=0, help="stack32k: layers in the stack (default: all 28)")
     p.add_argument("--kv-cap", type=int, default=0,
@@ -452,17 +455,19 @@ KV_ES = {"f32": 4, "bf16": 2, "fp8": 1}
 ATTN_ROWS = 32769  # the 32K-context attention of the 7B-shaped layer (pos 32768)
 
 
-def attn_kv_shape(synth):
+def attn_kv_shape(synth, rows=0):
     w = synth.WORKLOADS["7b8k"]
-    return w.H, w.KV, w.hd, ATTN_ROWS, ATTN_ROWS + 63
+    rows = rows or ATTN_ROWS
+    return w.H, w.KV, w.hd, rows, rows + 63
 
 
 def run_attn_kv(args, ws, pg, torch, q, synth, dev):
     """The decode attention of the 7B-shaped layer at 32,769 rows over an fp32,
     bf16 or fp8 E4M3 cache: one C-ABI attention call per step, calls back to
     back in a CUDA graph over replicated caches (more bytes than L2)."""
-    H, KV, hd, Tn, C = attn_kv_shape(synth)
+    H, KV, hd, Tn, C = attn_kv_shape(synth, args.rows)
     dt, es = args.kv_dtype, KV_ES[args.kv_dtype]
+    S = args.splits
     kv_bytes = 2 * KV * Tn * hd * es
     per_rep = 2 * KV * C * hd * es
     R = max(3, -(-int(2.5 * L2_BYTES) // per_rep))
@@ -481,7 +486,7 @@ def run_attn_kv(args, ws, pg, torch, q, synth, dev):
         reps.append((mk(), mk()))
     qv = torch.randn(H * hd, generator=gen, device=dev, dtype=torch.float32)
     out = torch.empty(H * hd, dtype=torch.float32, device=dev)
-    nbytes = q.ck_attn_scratch_size(H, KV, C, hd)
+    nbytes = max(q.ck_attn_scratch_size(H, KV, C, hd), q.ck_attn_split_scratch_size(H, KV, hd, max(S, 1)))
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -489,6 +494,9 @@ def run_attn_kv(args, ws, pg, torch, q, synth, dev):
         kc, vc = reps[i % R]
         qq = qv if qin is None else qin
         oo = out if o is None else o
+        if S >= 0:
+            return q.ck_attn_decode_gqa_split(qq, kc, vc, oo, H, KV, Tn, C, hd, {"f32": 0, "bf16": 1, "fp8": 2}[dt],
+                                              ks, vs, S, scratch, nbytes, stream.cuda_stream)
         if dt == "f32":
             return q.ck_attn_decode_gqa(qq, kc, vc, oo, H, KV, Tn, C, hd, scratch, nbytes, stream.cuda_stream)
         if dt == "bf16":
@@ -553,7 +561,8 @@ def run_attn_kv(args, ws, pg, torch, q, synth, dev):
             "dtype": {"f32": "f32", "bf16": "bf16 cache, f32 math", "fp8": "fp8 e4m3 cache, f32 math"}[dt],
             "data": "synthetic",
             "config": {"workload": f"attn32k: decode attention of the 28/4-head hd 128 layer over {Tn} rows of a "
-                                   f"{dt} cache (fp8: per-tensor scales {ks}, {vs}), one C-ABI call per step",
+                                   f"{dt} cache (fp8: per-tensor scales {ks}, {vs}), one C-ABI call per step"
+                                   + (f", ck_attn_decode_gqa_split with splits={S}" if S >= 0 else ""),
                        "l2": f"inputs larger than L2: {R} cache replicas rotated "
                              f"({R * per_rep / 2**20:.0f} MiB)"},
             "step_hbm_gbs": round(ach, 1), "step_bytes": kv_bytes,
@@ -565,15 +574,15 @@ def run_attn_kv(args, ws, pg, torch, q, synth, dev):
                     "how": "per call: pinned q -> device, the attention call, out -> pinned host"},
             "gpu_launches": 2 * K, "clocks": clocks}
     if not args.no_cpu_baseline and int(os.environ.get("RANK", "0")) == 0:
-        line["cpu_baseline"] = cpu_baseline_attn(synth, dt, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_attn(synth, dt, args.cpu_seconds, args.rows)
     return line
 
 
-def cpu_baseline_attn(synth, dt, budget_s):
+def cpu_baseline_attn(synth, dt, budget_s, rows=0):
     """The oracle attention over the same shape and cache type, calls until the budget."""
     import oracle
     oracle.lib()
-    H, KV, hd, Tn, C = attn_kv_shape(synth)
+    H, KV, hd, Tn, C = attn_kv_shape(synth, rows)
     rng = np.random.default_rng(7)
     qv = rng.standard_normal(H * hd).astype(np.float32)
     if dt == "fp8":
@@ -1106,7 +1115,7 @@ def run_reference(args, ws):
                 "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                             "d2h_bytes_per_step": 0}}
     if args.config == "attn32k":  # the oracle attention, as the CPU baseline
-        cb = cpu_baseline_attn(synth, args.kv_dtype, 60.0)
+        cb = cpu_baseline_attn(synth, args.kv_dtype, 60.0, args.rows)
         return {"impl": "reference", "metric": "decode attention calls/s and achieved HBM GB/s vs GB300 peak",
                 "value": cb["value"], "unit": "attention-calls/s", "n_gpus": ws, "steps": 1, "warmup": 0,
                 "ms_per_step": round(1e3 / cb["value"], 3), "higher_is_better": True, "scaling": "weak",

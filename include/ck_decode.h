@@ -141,8 +141,8 @@ int ck_attn_decode_gqa_noalloc(const float *q, const float *k_cache, const float
 
 /* ---- reduced-precision KV caches ---------------------------------------- */
 
-/* The same decode attention over a bf16 or an fp8 cache (page "paged
- * decode attention" launchers paged_decode_attn_bf16 / paged_decode_attn_fp8:
+/* The same decode attention over a bf16 or an fp8 cache (page
+ * "prefill_attn_a.rs", layers/ops: the launchers paged_decode_attn_bf16 / paged_decode_attn_fp8:
  * bf16 and fp8 KV caches, the fp8 one with per-tensor k_scale and v_scale;
  * here on the head-major layout of ck_attn_decode_gqa, not paged).
  * k_cache / v_cache: [num_kv_heads, cache_capacity, head_dim] elements of
@@ -160,6 +160,25 @@ int ck_attn_decode_gqa_fp8(const float *q, const void *k_cache, const void *v_ca
                            int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, float k_scale,
                            float v_scale, void *scratch, size_t scratch_bytes, void *stream);
 
+/* Split tuning.  The page "attn_v41/decode.rs" (spark_model layers) splits
+ * the output dimension of each head over several blocks when one block a
+ * head leaves SMs idle.  Here the same end is reached by splitting the
+ * attended rows (each split a partial softmax record, merged by a combine),
+ * which reads every row once; ck_attn_decode_gqa picks the split count from
+ * the SM count.  This entry point takes it explicitly, for tuning: the same
+ * attention as ck_attn_decode_gqa (kv_dtype 0), _bf16 (1) or _fp8 (2, with
+ * k_scale / v_scale; ignored otherwise) with `splits` splits of the rows per
+ * KV head, 1 <= splits <= 1024, or 0 for the built-in choice (otherwise
+ * CK_EINVAL).  Splits past the last row are empty and contribute nothing.
+ * `scratch`: >= ck_attn_split_scratch_size(num_heads, num_kv_heads,
+ * head_dim, splits) bytes (0 for invalid arguments); with splits = 0,
+ * ck_attn_scratch_size(...). */
+size_t ck_attn_split_scratch_size(int num_heads, int num_kv_heads, int head_dim, int splits);
+int ck_attn_decode_gqa_split(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                             int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_dtype,
+                             float k_scale, float v_scale, int splits, void *scratch, size_t scratch_bytes,
+                             void *stream);
+
 /* KV-cache store (page: STEP 6) into those caches: k_cache[h][pos][:] and
  * v_cache[h][pos][:] from the fp32 rows k, v [num_kv_heads * head_dim].
  * bf16: round to nearest, ties to even.  fp8: code = E4M3(x / scale) with x /
@@ -171,8 +190,8 @@ int ck_kv_store_bf16(void *k_cache, void *v_cache, const float *k, const float *
 int ck_kv_store_fp8(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
                     int cache_capacity, int head_dim, float k_scale, float v_scale, void *stream);
 
-/* Paged decode attention with an optional sliding window (page "paged decode
- * attention": paged_decode_attn_bf16 / paged_decode_attn_fp8 and their GQA
+/* Paged decode attention with an optional sliding window (page
+ * "prefill_attn_a.rs", layers/ops: paged_decode_attn_bf16 / paged_decode_attn_fp8 and their GQA
  * forms, arguments block_tables, seq_lens, max_blocks_per_seq, block_size,
  * sliding_window, k_scale, v_scale), for a batch of sequences.
  *   k_pool / v_pool: [num_blocks, num_kv_heads, block_size, head_dim]
@@ -299,7 +318,7 @@ size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim,
 
 /* ---- the multi-token (prefill) form of the layer ------------------------ */
 
-/* Page "C-Kernel-Engine" (kernel launchers): the prefill attention launcher,
+/* Page "prefill_attn_a.rs" (layers/ops): the prefill attention launcher,
  * one query per (head, token) with a causal switch.  Read here as the same
  * layer applied to `n_tokens` consecutive tokens of ONE sequence: token i sits
  * at position pos + i, its K / V rows are stored at row pos + i, and it

@@ -347,8 +347,8 @@ void ref_attention(const float *q, const float *k_cache, const float *v_cache, f
 }
 
 /* ------------------------------------------------------------------------
- * Reduced-precision KV caches (page "paged decode attention" launchers
- * paged_decode_attn_bf16 / paged_decode_attn_fp8: bf16 and fp8 caches, the
+ * Reduced-precision KV caches (page "prefill_attn_a.rs", layers/ops:
+ * the launchers paged_decode_attn_bf16 / paged_decode_attn_fp8: bf16 and fp8 caches, the
  * fp8 one with per-tensor k_scale and v_scale; the pages print only the
  * launchers, so the element formats are taken from their definitions):
  *
@@ -502,8 +502,8 @@ void ref_kv_store_kvq(void *k_cache, void *v_cache, const float *k, const float 
 }
 
 /* ------------------------------------------------------------------------
- * Paged decode attention with a sliding window (page "paged decode
- * attention": paged_decode_attn_bf16 / _fp8 and their GQA forms; only the
+ * Paged decode attention with a sliding window (page
+ * "prefill_attn_a.rs", layers/ops: paged_decode_attn_bf16 / _fp8 and their GQA forms; only the
  * launchers are printed).  Readings: the pools are [num_blocks][KV]
  * [block_size][hd]; row t of sequence b is row t % block_size of physical
  * block block_tables[b * max_blocks + t / block_size]; the sequence attends
@@ -630,8 +630,8 @@ void ref_decode_layer(float *out, const float *x, const float *residual, const u
 
 /* ------------------------------------------------------------------------
  * The multi-token (prefill) form of the same layer: n tokens of ONE sequence,
- * token i at position pos + i, causal.  Page "C-Kernel-Engine" (kernel
- * launchers), the prefill attention launcher: one query per (head, token)
+ * token i at position pos + i, causal.  Page "prefill_attn_a.rs"
+ * (layers/ops), the prefill attention launcher: one query per (head, token)
  * with a causal switch; read here as token i attending cache rows
  * 0 .. pos + i, i.e. the rows already in the cache plus the chunk's own rows
  * up to and including its own.

@@ -354,7 +354,7 @@ size_t ck_attn_scratch_size(int num_heads, int num_kv_heads, int max_kv_tokens, 
 
 static int attn_call(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
                      int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_type, float k_scale,
-                     float v_scale, void *scratch, size_t scratch_bytes, void *stream);
+                     float v_scale, void *scratch, size_t scratch_bytes, void *stream, int splits = 0);
 
 int ck_attn_decode_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int num_heads,
                        int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
@@ -378,6 +378,22 @@ int ck_attn_decode_gqa_fp8(const float *q, const void *k_cache, const void *v_ca
     if (!scale_ok(k_scale) || !scale_ok(v_scale)) return CK_EINVAL;
     return attn_call(q, k_cache, v_cache, out, num_heads, num_kv_heads, kv_tokens, cache_capacity, head_dim, KV_FP8,
                      k_scale, v_scale, scratch, scratch_bytes, stream);
+}
+
+size_t ck_attn_split_scratch_size(int num_heads, int num_kv_heads, int head_dim, int splits) {
+    if (attn_shape_ok(num_heads, num_kv_heads, head_dim) || splits < 1 || splits > 1024) return 0;
+    return attn_part_bytes(1, num_heads, num_kv_heads, head_dim, splits) + 256;
+}
+
+int ck_attn_decode_gqa_split(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
+                             int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_dtype,
+                             float k_scale, float v_scale, int splits, void *scratch, size_t scratch_bytes,
+                             void *stream) {
+    if (splits < 0 || splits > 1024 || kv_dtype < 0 || kv_dtype > 2) return CK_EINVAL;
+    if (kv_dtype == KV_FP8 && (!scale_ok(k_scale) || !scale_ok(v_scale))) return CK_EINVAL;
+    if (kv_dtype != KV_FP8) k_scale = v_scale = 1.0f;
+    return attn_call(q, k_cache, v_cache, out, num_heads, num_kv_heads, kv_tokens, cache_capacity, head_dim, kv_dtype,
+                     k_scale, v_scale, scratch, scratch_bytes, stream, splits);
 }
 
 static int kv_store_q(void *k_cache, void *v_cache, const float *k, const float *v, int pos, int num_kv_heads,
@@ -469,7 +485,7 @@ int ck_attn_decode_gqa_paged(const float *q, const void *k_pool, const void *v_p
 
 static int attn_call(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
                      int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, int kv_type, float k_scale,
-                     float v_scale, void *scratch, size_t scratch_bytes, void *stream) {
+                     float v_scale, void *scratch, size_t scratch_bytes, void *stream, int splits) {
     int rc = check_ptrs({q, k_cache, v_cache, out}, {});
     if (rc) return rc;
     if (kv_type != 0 && head_dim != 64 && head_dim != 128) return CK_EINVAL;
@@ -478,8 +494,8 @@ static int attn_call(const float *q, const void *k_cache, const void *v_cache, f
     if (kv_tokens < 1 || kv_tokens > cache_capacity) return CK_ERANGE;
     if (!scratch) return CK_ESCRATCH;
     if (!aligned16(scratch)) return CK_EALIGN;
-    // the split count follows the token count actually attended
-    const int S = attn_splits(1, num_kv_heads, kv_tokens);
+    // the split count follows the token count actually attended (or is given)
+    const int S = splits > 0 ? splits : attn_splits(1, num_kv_heads, kv_tokens);
     if (scratch_bytes < attn_part_bytes(1, num_heads, num_kv_heads, head_dim, S)) return CK_ESCRATCH;
     unsigned *st = status_word();
     if (!st) return CK_ECUDA;

@@ -1,7 +1,7 @@
 """Pins of the oracle's reduced-precision KV-cache functions (bf16 and fp8
-E4M3 caches, the latter with per-tensor k_scale / v_scale, as in the page
-"paged decode attention" launchers paged_decode_attn_bf16 /
-paged_decode_attn_fp8).  The element formats are pinned to values their
+E4M3 caches, the latter with per-tensor k_scale / v_scale, as in the
+launchers paged_decode_attn_bf16 / paged_decode_attn_fp8 of the page
+"prefill_attn_a.rs", layers/ops).  The element formats are pinned to values their
 definitions fix: E4M3 has 1 sign bit, 4 exponent bits with bias 7 and 3
 fraction bits, subnormals at exponent field 0 (frac * 2^-9), NaN at
 S.1111.111, no infinity and a largest finite magnitude of 448; bfloat16 is
