@@ -845,6 +845,42 @@ def run_prefill(args, ws, pg, torch, q, synth, dev):
     fl = prefill_attn_flops(P, n, w.H, w.hd)
     ach = fl * K / sec / 1e12
 
+    # the chunk's attention alone (ck_attn_prefill_gqa: K / V image + the
+    # tensor-core kernel), on the replicas' caches, calls in a CUDA graph
+    qa = torch.randn((n, w.H * w.hd), generator=gen, device=dev, dtype=torch.float32)
+    oa = torch.empty_like(qa)
+    anb = q.ck_attn_prefill_scratch_size(w.H, w.KV, w.hd, w.capacity)
+    asc = torch.empty(anb, dtype=torch.uint8, device=dev)
+
+    def attn(g):
+        q.check(q.ck_attn_prefill_gqa(qa, g["kc"], g["vc"], oa, P, n, w.H, w.KV, w.hd, w.capacity, asc, anb,
+                                      stream.cuda_stream))
+
+    ag = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ag, stream=stream):
+        for g in reps:
+            attn(g)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            ag.replay()
+    torch.cuda.synchronize()
+    Ka = max(1, K // R) * R
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a0.record(stream)
+        for _ in range(Ka // R):
+            ag.replay()
+        a1.record(stream)
+    a1.synchronize()
+    attn_ms = max_over_ranks(pg, torch, a0.elapsed_time(a1)) / Ka
+    attn_tf = fl / (attn_ms / 1e3) / 1e12
+    bf16_peak = 1941.2
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak, bf16_kind = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops (burst)"
+    except (OSError, KeyError, ValueError):
+        bf16_peak, bf16_kind = 1900.0, "fallback bf16"
+
     # e2e: the chunk's rows from pinned host memory, its output rows back
     Ke = min(K, 50)
     xh = torch.from_numpy(x0).pin_memory()
@@ -866,16 +902,21 @@ def run_prefill(args, ws, pg, torch, q, synth, dev):
     line = {"metric": "prefill tokens/s of the layer (causal chunk over the cache)",
             "value": round(ws * n * K / sec, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
             "ms_per_step": round(ms / K, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8/int5 codes: exact integer block dots (tcgen05 f16); fp32 attention", "data": "synthetic",
+            "dtype": "int8/int5 codes: exact integer block dots (tcgen05 f16); attention in bf16 hi/lo pairs "
+                     "(tcgen05, fp32 accumulation)", "data": "synthetic",
             "config": {"workload": f"prefill512: the D=3584 28/4-head hd=128 layer, tokens {P}..{P + n - 1} of one "
                                    f"sequence in one ck_prefill_layer call per step (causal: token i attends "
                                    f"{P} + i + 1 rows)",
                        "l2": f"{R} replicas of weights + caches ({per_rep / 1e6:.0f} MB each) in rotation"},
-            "attn_flops_per_step": fl,
-            "roofline": {"kernel": "whole prefill step (attention flops)", "bound": "alu",
-                         "achieved": round(ach, 2), "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
-                         "frac": round(ach / FP32_ALU_TFLOPS, 4),
-                         "peak_kind": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x 2.07 GHz", "traffic": None},
+            "attn_flops_per_step": fl, "step_attn_tflops": round(ach, 2),
+            "attn_alone": {"ms_per_call": round(attn_ms, 5), "calls": Ka,
+                           "how": "ck_attn_prefill_gqa on the same chunk and caches, calls in a CUDA graph"},
+            "roofline": {"kernel": "prefill attention (K/V image + tcgen05 kernel, one ck_attn_prefill_gqa call)",
+                         "bound": "tensor", "achieved": round(attn_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(attn_tf / bf16_peak, 4),
+                         "peak_kind": f"{bf16_kind}; the split-precision operands take 3 bf16 MMAs per product, "
+                                      f"so this kernel's algorithmic ceiling is 1/3 of the peak",
+                         "traffic": None},
             "e2e": {"value": round(ws * n * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": n * w.D * 4, "d2h_bytes_per_step": n * w.D * 4, "steps": Ke,
                     "how": "per step: pinned x [n, D] -> device, ck_prefill_layer, out -> pinned host"},

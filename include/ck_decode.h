@@ -324,7 +324,9 @@ size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim,
  * at position pos + i, its K / V rows are stored at row pos + i, and it
  * attends cache rows 0 .. pos + i (the rows already in the cache and the
  * chunk's own rows up to and including its own).  The result equals
- * n_tokens calls of ck_decode_layer at positions pos, pos + 1, ... in order.
+ * n_tokens calls of ck_decode_layer at positions pos, pos + 1, ... in order
+ * (head_dim 128: the attention as ck_attn_prefill_gqa, on the tensor cores;
+ * otherwise one decode attention per token).
  * out, x, residual: fp32 [n_tokens, embed_dim] (device; out must not alias x
  * or residual; residual may alias x).  k_cache, v_cache: head-major fp32
  * [num_kv_heads, cache_capacity, head_dim] (device, 16-byte aligned, else
@@ -336,6 +338,24 @@ size_t ck_decode_layer_batched_scratch_offset(int tap, int batch, int embed_dim,
  * `scratch`: >= ck_prefill_layer_scratch_size(...) bytes of device memory
  * (no initialization needed); the taps (CK_TAP_*) sit at
  * ck_prefill_layer_scratch_offset(...), row i for token i. */
+/* The chunk's attention alone (the prefill attention launcher of the same
+ * page: queries of every (token, head), causal), on the tensor cores.
+ * q, out: fp32 [n_tokens, num_heads * head_dim] (device, 16-byte aligned);
+ * token i (position pos + i) attends rows 0 .. pos + i of the head-major fp32
+ * caches [num_kv_heads, cache_capacity, head_dim], whose rows pos ..
+ * pos + n_tokens - 1 must already hold the chunk's K / V.  The result equals
+ * ck_attn_decode_gqa over pos + i + 1 rows for every token.  Operands are
+ * taken as bf16 pairs (hi + lo, about 17 significant bits) with fp32
+ * accumulation: a relative error near 1e-5 where the fp32 kernels reach 1e-7.
+ * Requirements: head_dim 128, num_heads a multiple of num_kv_heads with
+ * num_heads / num_kv_heads <= 16, 1 <= n_tokens
+ * <= 2^20 (else CK_EINVAL), 0 <= pos <= cache_capacity - n_tokens (else
+ * CK_ERANGE).  `scratch`: >= ck_attn_prefill_scratch_size(...) bytes (0 for
+ * unsupported shapes). */
+size_t ck_attn_prefill_scratch_size(int num_heads, int num_kv_heads, int head_dim, int cache_capacity);
+int ck_attn_prefill_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int pos,
+                        int n_tokens, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
+                        void *scratch, size_t scratch_bytes, void *stream);
 size_t ck_prefill_layer_scratch_size(int n_tokens, int embed_dim, int num_heads, int num_kv_heads, int head_dim,
                                      int cache_capacity);
 size_t ck_prefill_layer_scratch_offset(int tap, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,

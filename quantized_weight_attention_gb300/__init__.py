@@ -24,6 +24,7 @@ __all__ = [
     "ck_rope_inplace", "ck_kv_store", "ck_attn_scratch_size", "ck_attn_decode_gqa",
     "ck_prefill_layer_scratch_size", "ck_prefill_layer_scratch_offset", "ck_prefill_layer",
     "ck_attn_split_scratch_size", "ck_attn_decode_gqa_split",
+    "ck_attn_prefill_scratch_size", "ck_attn_prefill_gqa",
     "ck_decode_layer_scratch_size", "ck_decode_layer", "ck_decode_layer_devpos", "ck_device_status",
     "ck_block_dots_q5_0_q8_0", "ck_block_dots_q8_0_q8_0", "LIB_PATH", "ck_decode_layer_scratch_offset",
     "CK_TAP_Q", "CK_TAP_XQ8", "CK_TAP_ATTN", "CK_TAP_AQ8", "ck_attn_decode_gqa_noalloc",
@@ -76,6 +77,8 @@ _SIGS = {
     "ck_prefill_layer_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "ck_prefill_layer": (_I, [_P] * 16 + [_I] * 7 + [_F, _P, _SZ, _P]),
     "ck_attn_split_scratch_size": (_SZ, [_I, _I, _I, _I]),
+    "ck_attn_prefill_scratch_size": (_SZ, [_I, _I, _I, _I]),
+    "ck_attn_prefill_gqa": (_I, [_P] * 4 + [_I] * 6 + [_P, _SZ, _P]),
     "ck_attn_decode_gqa_split": (_I, [_P] * 4 + [_I] * 6 + [_F, _F, _I, _P, _SZ, _P]),
     "ck_block_dots_q5_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
     "ck_block_dots_q8_0_q8_0": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -278,6 +281,17 @@ def ck_decode_layer_batched_scratch_offset(tap: int, batch: int, embed_dim: int,
                                            head_dim: int, cache_capacity: int) -> int:
     return lib().ck_decode_layer_batched_scratch_offset(tap, batch, embed_dim, num_heads, num_kv_heads, head_dim,
                                                         cache_capacity)
+
+
+def ck_attn_prefill_scratch_size(num_heads: int, num_kv_heads: int, head_dim: int, cache_capacity: int) -> int:
+    return lib().ck_attn_prefill_scratch_size(num_heads, num_kv_heads, head_dim, cache_capacity)
+
+
+def ck_attn_prefill_gqa(q_, k_cache, v_cache, out, pos: int, n_tokens: int, num_heads: int, num_kv_heads: int,
+                        head_dim: int, cache_capacity: int, scratch, scratch_bytes: int, stream=None) -> int:
+    return lib().ck_attn_prefill_gqa(_ptr(q_), _ptr(k_cache), _ptr(v_cache), _ptr(out), pos, n_tokens, num_heads,
+                                     num_kv_heads, head_dim, cache_capacity, _ptr(scratch), scratch_bytes,
+                                     _stream(stream))
 
 
 def ck_attn_split_scratch_size(num_heads: int, num_kv_heads: int, head_dim: int, splits: int) -> int:

@@ -575,7 +575,8 @@ static int batched_body(float *out, const float *x, const float *residual, const
                         const float *bv, const float *bo, float *const *k_caches, float *const *v_caches,
                         const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch, int embed_dim,
                         int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps, uint8_t *sc,
-                        const BatchScratch &L, cudaStream_t s, bool pdl_first, int chunk_pos) {
+                        const BatchScratch &L, cudaStream_t s, bool pdl_first, int chunk_pos,
+                        uint8_t *pf_img = nullptr, float *pf_k = nullptr, float *pf_v = nullptr) {
     unsigned *st = status_word();
     if (!st) return CK_ECUDA;
 
@@ -646,7 +647,13 @@ static int batched_body(float *out, const float *x, const float *residual, const
     aa.l2_prefetch = wo;
     aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
     aa.status = st;
-    if (launch_attention(aa, batch, s, true, true)) return CK_ECUDA;
+    if (pf_img) {  // a prefill chunk on the tensor cores
+        if (launch_prefill_attn(aa, ba.q, pf_k, pf_v, pf_img, batch, chunk_pos, num_heads, num_kv_heads,
+                                cache_capacity, s))
+            return CK_ECUDA;
+    } else if (launch_attention(aa, batch, s, true, true)) {
+        return CK_ECUDA;
+    }
     if ((tc ? launch_rows_tc(ba, true, s, true) : launch_rows_batched(ba, true, s, true))) return CK_ECUDA;
     return CK_OK;
 }
@@ -676,7 +683,8 @@ int ck_decode_layer_batched(float *out, const float *x, const float *residual, c
 // per-entry cache pointers and positions live after the batched scratch.
 struct PrefillScratch {
     BatchScratch b;
-    size_t off_kcs, off_vcs, off_pos, total;
+    size_t off_kcs, off_vcs, off_pos, off_img, total;
+    bool tc_attn;  // the chunk's attention on the tensor cores (else one decode attention per token)
 };
 
 static PrefillScratch prefill_scratch(int n, int D, int H, int KV, int hd, int C) {
@@ -689,6 +697,9 @@ static PrefillScratch prefill_scratch(int n, int D, int H, int KV, int hd, int C
     o = a256(o + static_cast<size_t>(n) * sizeof(float *));
     P.off_pos = o;
     o = a256(o + static_cast<size_t>(n) * 4);
+    P.tc_attn = prefill_tc_ok(H, KV, hd) && batched_tc_ok(D, H, KV, hd);
+    P.off_img = o;
+    if (P.tc_attn) o = a256(o + prefill_img_bytes(KV, C));
     P.total = o;
     return P;
 }
@@ -703,6 +714,40 @@ size_t ck_prefill_layer_scratch_offset(int tap, int n_tokens, int embed_dim, int
                                        int head_dim, int cache_capacity) {
     return ck_decode_layer_batched_scratch_offset(tap, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim,
                                                   cache_capacity);
+}
+
+size_t ck_attn_prefill_scratch_size(int num_heads, int num_kv_heads, int head_dim, int cache_capacity) {
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || cache_capacity <= 0) return 0;
+    if (!prefill_tc_ok(num_heads, num_kv_heads, head_dim)) return 0;
+    return prefill_img_bytes(num_kv_heads, cache_capacity) + 256;
+}
+
+int ck_attn_prefill_gqa(const float *q, const float *k_cache, const float *v_cache, float *out, int pos,
+                        int n_tokens, int num_heads, int num_kv_heads, int head_dim, int cache_capacity,
+                        void *scratch, size_t scratch_bytes, void *stream) {
+    int rc = check_ptrs({q, k_cache, v_cache, out}, {});
+    if (rc) return rc;
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return CK_EINVAL;
+    if (!prefill_tc_ok(num_heads, num_kv_heads, head_dim) || cache_capacity <= 0 || n_tokens < 1 ||
+        n_tokens > (1 << 20))
+        return CK_EINVAL;
+    if (pos < 0 || pos > cache_capacity - n_tokens) return CK_ERANGE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return CK_EALIGN;
+    if (!scratch) return CK_ESCRATCH;
+    if (!aligned16(scratch)) return CK_EALIGN;
+    if (scratch_bytes < prefill_img_bytes(num_kv_heads, cache_capacity)) return CK_ESCRATCH;
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
+    AttnArgs o{};
+    o.H = num_heads;
+    o.KV = num_kv_heads;
+    o.hd = head_dim;
+    o.out = out;
+    o.status = st;
+    return launch_prefill_attn(o, q, k_cache, v_cache, static_cast<uint8_t *>(scratch), n_tokens, pos, num_heads,
+                               num_kv_heads, cache_capacity, as_stream(stream))
+               ? CK_ECUDA
+               : CK_OK;
 }
 
 int ck_prefill_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
@@ -730,7 +775,7 @@ int ck_prefill_layer(float *out, const float *x, const float *residual, const vo
     // the first batched launch waits for the whole setup grid (no overlap)
     return batched_body(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, kcs, vcs, rope_cos, rope_sin,
                         pos_of, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps, sc,
-                        P.b, s, false, pos);
+                        P.b, s, false, pos, P.tc_attn ? sc + P.off_img : nullptr, k_cache, v_cache);
 }
 
 size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,

@@ -147,6 +147,14 @@ size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
 int attn_splits(int B, int KV, int max_tokens);
 int attn_splits_batched(int B, int KV, int max_tokens);
 int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine);
+// Prefill attention on the tensor cores (head_dim 128, query groups up to 16):
+// the chunk's rows of KV head g against cache rows 0 .. pos + n - 1, causal;
+// outputs through the decode attention's store (o.out, o.out_q8, o.out_img,
+// o.out_pack).  img: prefill_img_bytes(KV, C) bytes of scratch.
+bool prefill_tc_ok(int H, int KV, int hd);
+size_t prefill_img_bytes(int KV, int C);
+int launch_prefill_attn(const AttnArgs &o, const float *q, const float *k_cache, const float *v_cache, uint8_t *img,
+                        int n, int pos, int H, int KV, int C, cudaStream_t s);
 int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, int H, int KV, int hd, cudaStream_t s);
 int launch_kv_store(float *kc, float *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
                     cudaStream_t s);

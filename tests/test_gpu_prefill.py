@@ -4,8 +4,13 @@ The chunk's tokens must match the oracle's prefill form token by token, under
 the layer's tolerances: bit-exact Q8_0 activations; max |err| <= 1e-3 * max |ref|
 and relative L2 <= 1e-4 for floats.  The O-projection input is checked in
 situ: it must be the oracle quantizer applied to the GPU's own attention
-output.  Cache rows from pos + n_tokens on are NaN, so a read of a row that is
-not yet part of the sequence shows up in the results."""
+output.  A code of that input may legitimately differ from the oracle's where
+the two attention outputs straddle a rounding boundary (one step of a block's
+scale d); the layer output is then checked against the oracle's O projection
+of the GPU's own codes, and end to end wherever no code differs, and the
+number of differing codes is bounded.  Cache rows from pos + n_tokens on are
+NaN, so a read of a row that is not yet part of the sequence shows up in the
+results."""
 import dataclasses
 
 import numpy as np
@@ -43,6 +48,10 @@ def dev(cuda_ok):
 
 def T(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def H_(t):
+    return H(t)
 
 
 def H(t):
@@ -108,13 +117,23 @@ class Chunk:
         assert np.array_equal(xq, taps["xq"]), "quantized inputs"
         assert np.array_equal(gk[:, :p], self.kc0[:, :p]) and np.array_equal(gv[:, :p], self.vc0[:, :p]), "old rows"
         assert np.all(np.isnan(gk[:, p + n:])) and np.all(np.isnan(gv[:, p + n:])), "rows past the chunk"
+        flips = 0
         for i in range(n):
             assert_close(qt[i], taps["q"][i], f"token {i}: q")
             assert_close(gk[:, p + i].ravel(), taps["k"][i], f"token {i}: stored k")
             assert_close(gv[:, p + i].ravel(), taps["v"][i], f"token {i}: stored v")
             assert_close(at[i], taps["attn"][i], f"token {i}: attention output")
             assert np.array_equal(aq[i], oracle.quantize_q8_0(at[i])), f"token {i}: O-projection input"
-            assert_close(out[i], ref[i], f"token {i}: layer output")
+            # the O projection + bias + residual on the GPU's own codes
+            stage = oracle.gemv(self.wo, aq[i], self.bo, w.D, w.QD, False) + self.x[i]
+            assert_close(out[i], stage, f"token {i}: layer output (O projection of its own codes)")
+            codes_g = aq[i].reshape(-1, 34)[:, 2:]
+            codes_o = taps["aq"][i].reshape(-1, 34)[:, 2:]
+            nf = int(np.count_nonzero(codes_g != codes_o))
+            flips += nf
+            if nf == 0:
+                assert_close(out[i], ref[i], f"token {i}: layer output")
+        assert flips <= max(2, n * w.QD // 500), f"{flips} O-projection input codes differ from the oracle's"
         rc, st = q.ck_device_status()
         assert rc == 0 and st == 0
 
@@ -219,3 +238,60 @@ def test_prefill_argument_errors(dev):
     assert np.all(H(c.out) == 3.0)
     assert np.array_equal(H(c.kc), c.kc0, equal_nan=True)
     assert q.ck_prefill_layer_scratch_size(0, w.D, w.H, w.KV, w.hd, w.capacity) == 0
+
+
+@pytest.mark.parametrize("D,H,KV,pos,n,C", [
+    (3584, 28, 4, 0, 1, 256),     # one token, no prefix
+    (3584, 28, 4, 0, 16, 256),    # exactly one 128-row query tile (16 tokens x 8 head slots)
+    (3584, 28, 4, 5, 17, 256),    # a second tile holding one token
+    (3584, 28, 4, 100, 64, 200),  # ends at row 163 of a 200-row cache: ragged last key tile
+    (2048, 16, 4, 333, 70, 512),  # query groups of 4 (32 tokens per tile)
+    (2048, 16, 2, 50, 20, 128),   # groups of 8 over two KV heads
+])
+def test_prefill_tensor_core_attention_shapes(dev, D, H, KV, pos, n, C):
+    """head_dim 128: the chunk's attention runs on the tensor cores; tiles of
+    query rows and key rows with ragged ends, several group sizes."""
+    w = dataclasses.replace(synth.WORKLOADS["7b8k"], D=D, H=H, KV=KV, hd=128, capacity=C)
+    c = Chunk(dev, w, pos, n, seed=91 + n + pos)
+    ok(c.call())
+    c.check()
+
+
+@pytest.mark.parametrize("H,KV,pos,n,C", [(28, 4, 0, 1, 64), (28, 4, 130, 33, 200), (16, 2, 7000, 300, 7300),
+                                          (8, 8, 10, 70, 96), (32, 2, 64, 64, 128)])
+def test_attn_prefill_alone(dev, H, KV, pos, n, C):
+    """ck_attn_prefill_gqa against the oracle's decode attention over pos + i + 1
+    rows for every token (groups of 7, 8, 1 and 16; a 7,300-row cache)."""
+    hd = 128
+    rng = np.random.default_rng(pos + n + H)
+    kc0 = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    vc0 = rng.standard_normal((KV, C, hd)).astype(np.float32)
+    kc0[:, pos + n:] = np.nan
+    vc0[:, pos + n:] = np.nan
+    qv = (rng.standard_normal((n, H * hd)) * 1.5).astype(np.float32)
+    nb = q.ck_attn_prefill_scratch_size(H, KV, hd, C)
+    assert nb > 0
+    sc = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = torch.full((n, H * hd), float("nan"), dtype=torch.float32, device=dev)
+    ok(q.ck_attn_prefill_gqa(T(qv, dev), T(kc0, dev), T(vc0, dev), out, pos, n, H, KV, hd, C, sc, nb))
+    got = H_(out)
+    for i in sorted({0, n // 2, n - 1} | set(range(0, n, max(1, n // 12)))):
+        ref = oracle.attention(qv[i], kc0, vc0, H, KV, pos + i + 1, C, hd)
+        assert_close(got[i], ref, f"token {i}")
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0
+
+
+def test_attn_prefill_argument_errors(dev):
+    H, KV, hd, C = 28, 4, 128, 64
+    z = torch.zeros((KV, C, hd), dtype=torch.float32, device=dev)
+    qv = torch.zeros((8, H * hd), dtype=torch.float32, device=dev)
+    out = torch.zeros_like(qv)
+    nb = q.ck_attn_prefill_scratch_size(H, KV, hd, C)
+    sc = torch.empty(nb, dtype=torch.uint8, device=dev)
+    f = lambda pos=0, n=8, hd_=hd, bytes_=nb: q.ck_attn_prefill_gqa(qv, z, z, out, pos, n, H, KV, hd_, C, sc, bytes_)
+    assert f(pos=57) == q.CK_ERANGE and f(pos=-1) == q.CK_ERANGE
+    assert f(n=0) == q.CK_EINVAL and f(hd_=64) == q.CK_EINVAL
+    assert f(bytes_=nb - 257) == q.CK_ESCRATCH
+    assert q.ck_attn_prefill_scratch_size(H, KV, 64, C) == 0
+    ok(f(pos=56))
