@@ -9,9 +9,10 @@
 //   S  = Q K^T        (M 128, N 64, K = head_dim 128) into TMEM
 //   P  = exp2(S - m)  (one thread per query row, the online softmax)
 //   O += P V          (M 128, N 128, K 64) accumulated in TMEM
-// Every fp32 operand x is held exactly enough as two bf16 numbers,
-// x = hi + lo + O(2^-17 |x|); a product takes three MMAs (hi.hi, hi.lo,
-// lo.hi) with fp32 accumulation.  The row maximum m is raised only when a
+// Q and P are the A operands and live in TMEM (each query row's lane), K and
+// V^T stream through shared memory.  Every fp32 operand x is held as two
+// bf16 numbers, x = hi + lo + O(2^-17 |x|); a product takes three MMAs
+// (hi.hi, hi.lo, lo.hi) with fp32 accumulation.  The row maximum m is raised only when a
 // tile's maximum exceeds it by more than 2^8 (in exp2 units), so O and the
 // row sum are rescaled rarely; p stays below 256.
 //
@@ -31,20 +32,19 @@ namespace {
 constexpr int PF_M = 128;  // query rows per CTA
 constexpr int PF_N = 64;   // key rows per tile
 constexpr int PF_HD = 128;
-constexpr int PF_Q_PART = PF_M * PF_HD * 2;  // bytes of one bf16 part of the Q tile
 constexpr int PF_K_PART = PF_N * PF_HD * 2;
 constexpr int PF_V_PART = PF_HD * PF_N * 2;
-constexpr int PF_P_PART = PF_M * PF_N * 2;
 constexpr int PF_TILE = 2 * PF_K_PART + 2 * PF_V_PART;  // one key tile of the image
-constexpr int PF_NST = 2;                                // key tiles in flight
+constexpr int PF_NST = 3;                                // key tiles in flight
 constexpr int PF_THREADS = 192;                          // warps 0-3 rows, 4 copies, 5 MMA
-constexpr int PF_TMEM_COLS = 256;                        // S slots 0-63, 64-127; O 128-255
 constexpr float PF_TAU = 8.0f;
+// TMEM columns (lane = query row): Q hi / lo as bf16 pairs (64 + 64), the two
+// S slots (64 fp32 each), the two P buffers (hi 32 + lo 32 each), O (128 fp32)
+constexpr int TC_Q = 0, TC_S = 128, TC_P = 256, TC_O = 384;
+constexpr int PF_TMEM_COLS = 512;
 
-constexpr size_t PF_OFF_Q = 0;
-constexpr size_t PF_OFF_KV = PF_OFF_Q + 2 * PF_Q_PART;
-constexpr size_t PF_OFF_P = PF_OFF_KV + static_cast<size_t>(PF_NST) * PF_TILE;
-constexpr size_t PF_OFF_BAR = PF_OFF_P + 2 * PF_P_PART;
+constexpr size_t PF_OFF_KV = 0;
+constexpr size_t PF_OFF_BAR = PF_OFF_KV + static_cast<size_t>(PF_NST) * PF_TILE;
 constexpr size_t PF_OFF_TMEM = PF_OFF_BAR + 16 * 8;
 constexpr size_t PF_SMEM = PF_OFF_TMEM + 16;
 static_assert(PF_SMEM <= 227 * 1024, "shared memory");
@@ -100,11 +100,13 @@ __device__ __forceinline__ void tm_wait_st() { asm volatile("tcgen05.wait::st.sy
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void pf_mma(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, bool acc) {
+// One MMA, D (TMEM) += A x B, A read from TMEM (`a_tmem`: lane = row of A,
+// each 32-bit column two consecutive K elements), B from shared memory.
+__device__ __forceinline__ void pf_mma_ts(uint32_t dtmem, uint32_t a_tmem, uint64_t bd, uint32_t idesc, bool acc) {
     asm volatile(
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(dtmem),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(dtmem),
+        "r"(a_tmem), "l"(bd), "r"(idesc), "r"(static_cast<uint32_t>(acc))
         : "memory");
 }
 __device__ __forceinline__ void pf_commit(uint64_t *bar) {
@@ -175,10 +177,10 @@ __global__ void __launch_bounds__(256) k_pf_kv_image(const PfArgs a) {
 
 __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *sq = smem + PF_OFF_Q, *skv = smem + PF_OFF_KV, *sp = smem + PF_OFF_P;
+    uint8_t *skv = smem + PF_OFF_KV;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + PF_OFF_BAR);
-    uint64_t *kv_full = bars, *kv_empty = bars + 2, *s_full = bars + 4, *p_full = bars + 6, *o_full = bars + 7,
-             *q_ready = bars + 8;
+    uint64_t *kv_full = bars, *kv_empty = bars + PF_NST, *s_full = bars + 2 * PF_NST, *p_full = s_full + 2,
+             *o_full = p_full + 2, *q_ready = o_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + PF_OFF_TMEM);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.y;
@@ -190,10 +192,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
         for (int i = 0; i < PF_NST; ++i) {
             mbar_init(kv_full + i, 1);
             mbar_init(kv_empty + i, 1);
-            mbar_init(s_full + i, 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(p_full + i, 4);
+            mbar_init(o_full + i, 1);
+        }
         mbar_init(q_ready, 4);
         fence_mbar_init();
     }
@@ -216,32 +220,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
         const int tl = tl0 + r / a.GP, hs = r % a.GP;
         const bool valid = tl < a.n && hs < a.G;
         const int limit = a.pos + min(tl, a.n - 1);  // the last key row this row sees
-        {
+        const uint32_t lanes = taddr + (static_cast<uint32_t>(warp * 32) << 16);
+        {  // the row's q as bf16 hi / lo into its TMEM lane (the A operand of S)
             const float4 *qr = reinterpret_cast<const float4 *>(
                 a.q + (static_cast<size_t>(valid ? tl : 0) * a.H + g * a.G + (valid ? hs : 0)) * PF_HD);
-#pragma unroll 4
-            for (int c = 0; c < PF_HD / 8; ++c) {
-                float x[8];
-                const float4 u = valid ? qr[2 * c] : make_float4(0.f, 0.f, 0.f, 0.f);
-                const float4 w = valid ? qr[2 * c + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
-                x[0] = u.x, x[1] = u.y, x[2] = u.z, x[3] = u.w, x[4] = w.x, x[5] = w.y, x[6] = w.z, x[7] = w.w;
-                uint4 hi, lo;
-                bf_split8(x, hi, lo);
-                const int off = cm_off(r, 8 * c, PF_HD);
-                *reinterpret_cast<uint4 *>(sq + off) = hi;
-                *reinterpret_cast<uint4 *>(sq + PF_Q_PART + off) = lo;
+#pragma unroll 1
+            for (int ch = 0; ch < PF_HD / 32; ++ch) {
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float x[8];
+                    const float4 u = valid ? qr[8 * ch + 2 * c] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 w = valid ? qr[8 * ch + 2 * c + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[0] = u.x, x[1] = u.y, x[2] = u.z, x[3] = u.w, x[4] = w.x, x[5] = w.y, x[6] = w.z, x[7] = w.w;
+                    uint4 hi, lo;
+                    bf_split8(x, hi, lo);
+                    hw[4 * c] = hi.x, hw[4 * c + 1] = hi.y, hw[4 * c + 2] = hi.z, hw[4 * c + 3] = hi.w;
+                    lw[4 * c] = lo.x, lw[4 * c + 1] = lo.y, lw[4 * c + 2] = lo.z, lw[4 * c + 3] = lo.w;
+                }
+                tm_st16(lanes + TC_Q + 16 * ch, hw);
+                tm_st16(lanes + TC_Q + PF_HD / 2 + 16 * ch, lw);
             }
+            tm_wait_st();
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_ready);
 
-        const uint32_t lanes = taddr + (static_cast<uint32_t>(warp * 32) << 16);
         float m = -INFINITY, l = 0.0f;  // exp2 units
         bool ok = true;
         for (int j = 0; j < nkt; ++j) {
+            const int b = j & 1;
             // (wait results made warp-uniform: the TMEM accesses are warp-wide)
-            if (!__all_sync(0xffffffffu, mbar_wait(s_full + (j & 1), (j >> 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(s_full + b, (j >> 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -250,7 +261,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
             {
                 uint32_t v[PF_N / 16][16];
 #pragma unroll
-                for (int c = 0; c < PF_N / 16; ++c) tm_ld16(lanes + (j & 1) * PF_N + 16 * c, v[c]);
+                for (int c = 0; c < PF_N / 16; ++c) tm_ld16(lanes + TC_S + b * PF_N + 16 * c, v[c]);
                 tm_wait_ld();
 #pragma unroll
                 for (int c = 0; c < PF_N / 16; ++c)
@@ -280,42 +291,51 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
                 ps += p[c];
             }
             l += ps;
-            if (j > 0) {  // P.V of the previous tile is done: P's buffer is free, O is stable
-                if (!__all_sync(0xffffffffu, mbar_wait(o_full, (j - 1) & 1))) {
+            if (__any_sync(0xffffffffu, rescale)) {  // O must hold every earlier tile's P.V first
+                if (!__all_sync(0xffffffffu, mbar_wait(o_full + (b ^ 1), ((j - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v[16];
+#pragma unroll 1
+                for (int c = 0; c < PF_HD / 16; ++c) {
+                    tm_ld16(lanes + TC_O + 16 * c, v);
+                    tm_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                    tm_st16(lanes + TC_O + 16 * c, v);
+                }
+            }
+            if (j >= 2) {  // P buffer b was last read by the P.V of tile j - 2
+                if (!__all_sync(0xffffffffu, mbar_wait(o_full + b, ((j - 2) >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
             }
-            if (__any_sync(0xffffffffu, rescale)) {
-                uint32_t v[16];
-#pragma unroll 1
-                for (int c = 0; c < PF_HD / 16; ++c) {
-                    tm_ld16(lanes + 2 * PF_N + 16 * c, v);
-                    tm_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                    tm_st16(lanes + 2 * PF_N + 16 * c, v);
+            for (int h = 0; h < PF_N / 32; ++h) {
+                uint32_t hw[16], lw[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = p[32 * h + 8 * c + i];
+                    uint4 hi, lo;
+                    bf_split8(x, hi, lo);
+                    hw[4 * c] = hi.x, hw[4 * c + 1] = hi.y, hw[4 * c + 2] = hi.z, hw[4 * c + 3] = hi.w;
+                    lw[4 * c] = lo.x, lw[4 * c + 1] = lo.y, lw[4 * c + 2] = lo.z, lw[4 * c + 3] = lo.w;
                 }
-                tm_wait_st();
+                tm_st16(lanes + TC_P + b * PF_N + 16 * h, hw);
+                tm_st16(lanes + TC_P + b * PF_N + PF_N / 2 + 16 * h, lw);
             }
-#pragma unroll
-            for (int c = 0; c < PF_N / 8; ++c) {
-                float x[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = p[8 * c + i];
-                uint4 hi, lo;
-                bf_split8(x, hi, lo);
-                const int off = cm_off(r, 8 * c, PF_N);
-                *reinterpret_cast<uint4 *>(sp + off) = hi;
-                *reinterpret_cast<uint4 *>(sp + PF_P_PART + off) = lo;
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tm_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full + b);
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full, (nkt - 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_full + ((nkt - 1) & 1), ((nkt - 1) >> 1) & 1));
         if (!ok) flag_error(a.o.status, FLAG_TIMEOUT);
         tc_fence_after();
         // ---- output rows: O / l staged in shared memory (the key stages are
@@ -327,7 +347,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
             uint32_t v[16];
 #pragma unroll 1
             for (int c = 0; c < PF_HD / 16; ++c) {
-                tm_ld16(lanes + 2 * PF_N + 16 * c, v);
+                tm_ld16(lanes + TC_O + 16 * c, v);
                 tm_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -344,12 +364,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
                 combine_store<PF_HD>(a.o, t2, g * a.G + h2, blk, lane, stg[rr * (PF_HD + 1) + blk * 32 + lane]);
         }
     } else if (warp == 4) {
-        // ---- copies: key tile j into stage j % 2 once the MMAs of tile j - 2 are done
+        // ---- copies: key tile j into stage j % 3 once the MMAs of tile j - 3 are done
         if (lane == 0) {
             const uint8_t *src = a.img + static_cast<size_t>(g) * a.ntk * PF_TILE;
             for (int j = 0; j < nkt; ++j) {
-                const int st = j & 1;
-                if (j >= PF_NST && !mbar_wait(kv_empty + st, ((j >> 1) - 1) & 1)) {
+                const int st = j % PF_NST;
+                if (j >= PF_NST && !mbar_wait(kv_empty + st, ((j / PF_NST) - 1) & 1)) {
                     flag_error(a.o.status, FLAG_TIMEOUT);
                     break;
                 }
@@ -360,25 +380,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
         }
         __syncwarp();
     } else {
-        // ---- MMA issue: S of tile j + 1 goes in before P.V of tile j
+        // ---- MMA issue: S of tile j + 1 goes in before P.V of tile j.  The A
+        // operands (Q, P) are read from TMEM, the B operands (K, V^T) from
+        // the stages.
         if (lane == 0) {
             constexpr uint32_t IDS = pf_idesc(PF_M, PF_N), IDO = pf_idesc(PF_M, PF_HD);
-            const uint64_t qd = pf_desc(sptr(sq), PF_HD * 16), pd = pf_desc(sptr(sp), PF_N * 16);
             auto issue_s = [&](int j) -> bool {
-                const int st = j & 1;
-                if (!mbar_wait(kv_full + st, (j >> 1) & 1)) return false;
+                const int st = j % PF_NST;
+                if (!mbar_wait(kv_full + st, (j / PF_NST) & 1)) return false;
                 tc_fence_after();
                 const uint64_t kd = pf_desc(sptr(skv + static_cast<size_t>(st) * PF_TILE), PF_HD * 16);
-                const uint32_t d = taddr + st * PF_N;
+                const uint32_t d = taddr + TC_S + (j & 1) * PF_N;
 #pragma unroll
                 for (int ks = 0; ks < PF_HD / 16; ++ks)
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {  // hi.hi, hi.lo, lo.hi
-                        const uint64_t ad = qd + (term == 2 ? PF_Q_PART / 16 : 0) + ks * 16;
+                        const uint32_t at = taddr + TC_Q + (term == 2 ? PF_HD / 2 : 0) + ks * 8;
                         const uint64_t bd = kd + (term == 1 ? PF_K_PART / 16 : 0) + ks * 16;
-                        pf_mma(d, ad, bd, IDS, ks > 0 || term > 0);
+                        pf_mma_ts(d, at, bd, IDS, ks > 0 || term > 0);
                     }
-                pf_commit(s_full + st);
+                pf_commit(s_full + (j & 1));
                 return true;
             };
             bool ok = mbar_wait(q_ready, 0);
@@ -388,19 +409,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
             }
             for (int j = 0; j < nkt && ok; ++j) {
                 if (j + 1 < nkt && !(ok = issue_s(j + 1))) break;
-                if (!(ok = mbar_wait(p_full, j & 1))) break;
+                const int b = j & 1;
+                if (!(ok = mbar_wait(p_full + b, (j >> 1) & 1))) break;
                 tc_fence_after();
-                const int st = j & 1;
+                const int st = j % PF_NST;
                 const uint64_t vd = pf_desc(sptr(skv + static_cast<size_t>(st) * PF_TILE + 2 * PF_K_PART), PF_N * 16);
 #pragma unroll
                 for (int ks = 0; ks < PF_N / 16; ++ks)
 #pragma unroll
                     for (int term = 0; term < 3; ++term) {
-                        const uint64_t ad = pd + (term == 2 ? PF_P_PART / 16 : 0) + ks * 16;
+                        const uint32_t at = taddr + TC_P + b * PF_N + (term == 2 ? PF_N / 2 : 0) + ks * 8;
                         const uint64_t bd = vd + (term == 1 ? PF_V_PART / 16 : 0) + ks * 16;
-                        pf_mma(taddr + 2 * PF_N, ad, bd, IDO, j > 0 || ks > 0 || term > 0);
+                        pf_mma_ts(taddr + TC_O, at, bd, IDO, j > 0 || ks > 0 || term > 0);
                     }
-                pf_commit(o_full);
+                pf_commit(o_full + b);
                 pf_commit(kv_empty + st);
             }
             if (!ok) flag_error(a.o.status, FLAG_TIMEOUT);
