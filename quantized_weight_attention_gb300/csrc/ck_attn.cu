@@ -100,6 +100,7 @@ extern template int launch_attention_dpl<2, KV_FP8>(const AttnArgs &, int, cudaS
 extern template int launch_attention_dpl<4, KV_FP8>(const AttnArgs &, int, cudaStream_t, bool, bool);
 
 int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine) {
+    if (attention_tc_ok(a.kv_type, a.H, a.KV, a.hd)) return launch_attention_tc(a, B, s, pdl_first, pdl_combine);
     if (a.kv_type == KV_BF16 || a.kv_type == KV_FP8) {  // head_dim 64 and 128
         const bool f8 = a.kv_type == KV_FP8;
         switch (a.hd) {

@@ -147,6 +147,10 @@ size_t attn_part_bytes(int B, int H, int KV, int hd, int splits);
 int attn_splits(int B, int KV, int max_tokens);
 int attn_splits_batched(int B, int KV, int max_tokens);
 int launch_attention(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine);
+// bf16 / fp8 caches at head_dim 128, query groups up to 8: the split kernel
+// with its scores on the tensor cores (same records, same combine).
+bool attention_tc_ok(int kv_type, int H, int KV, int hd);
+int launch_attention_tc(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first, bool pdl_combine);
 // Prefill attention on the tensor cores (head_dim 128, query groups up to 16):
 // the chunk's rows of KV head g against cache rows 0 .. pos + n - 1, causal;
 // outputs through the decode attention's store (o.out, o.out_q8, o.out_img,
