@@ -9,20 +9,22 @@
 //                 exact in bf16), B = q in shared memory as three bf16 parts
 //                 q1 + q2 + q3 (24 significant bits); six independent
 //                 accumulators (q part x half of the dims), summed by the rows
-//   softmax       one thread per row; each row warp keeps its own running
-//                 maximum per head over its rows (warp shuffles only), raised
-//                 only when a tile's exceeds it by more than 2^8 (exp2 units)
-//   O += P V      CUDA cores: a lane owns 4 of the 128 dims, a warp its 32
-//                 rows of the tile, p read from shared memory as a broadcast
+//   softmax       one thread per row
+//   O^T += V^T P^T (M = 128 dims, N = 16 head slots, K = 128 rows): A = the
+//                 tile's V transposed into TMEM (each dim's lane, exact bf16),
+//                 B = p in shared memory as bf16 hi + lo parts
 // Two groups of four row warps take alternate tiles, each with its own TMEM
-// K and S buffers; a group stores the K rows of its next tile as soon as it
-// has read this tile's scores, so the MMAs of one tile run under the
-// softmax and P V of another.  K and V rows come in separate rings: a K slot
-// is free once its rows are in TMEM, a V slot once P V has read it.  The
-// eight warps' states merge once at the end.
+// K, S, V^T and O^T buffers and its own softmax state (the four warps agree
+// on a running maximum per head through a per-tile exchange; it is raised
+// only when a tile's exceeds it by more than 2^8, exp2 units, and O^T and
+// the row sums are then rescaled).  A group stores the K rows of its next
+// tile as soon as it has read this tile's scores.  K and V rows come in
+// separate rings: a slot is free once its rows are in TMEM.  The two groups'
+// states merge once at the end.
 // Warp roles: 0 copies (lane 0 K rows, lane 1 V rows; contiguous or as runs
-// inside paged blocks), 1-8 rows (group (warp - 1) / 4), 9 MMA issue (and
-// TMEM).
+// inside paged blocks), 1-8 rows (group (warp - 1) / 4), 9 the score MMAs
+// (and TMEM), 10 the P V MMAs.  fp8 caches take P V in fp16 (E4M3 values
+// and p's hi / lo parts are exact there), bf16 caches in bf16.
 #include <cuda_bf16.h>
 
 #include "ck_attn_kernels.cuh"
@@ -34,14 +36,17 @@ constexpr int TA_HD = 128;
 constexpr int TA_M = 128;                   // rows per tile
 constexpr int TA_N = 16;                    // head slots (MMA N)
 constexpr int TA_RW = 8;                    // row warps (two groups of four)
-constexpr int TA_THREADS = 32 * (TA_RW + 2);
+constexpr int TA_THREADS = 32 * (TA_RW + 3);
 constexpr int TA_QPART = TA_N * TA_HD * 2;  // one bf16 part of the q image
 constexpr int TA_RING = 192 * 1024;         // K and V rings together
-// TMEM columns: a K buffer per group (64 columns of bf16 pairs), then an S
-// buffer per group of six partial accumulators (16 columns each)
+// TMEM columns per group gi: K rows (64 columns of bf16 pairs), the six
+// partial score accumulators (16 columns each), V^T (64 columns of bf16
+// pairs over the tile's rows) and O^T (16 columns)
 constexpr int TA_NACC = 6;
 constexpr int TA_TMEM_COLS = 512;
-constexpr int TC_K = 0, TC_S = 2 * (TA_HD / 2);
+constexpr int TC_K = 0, TC_S = 2 * (TA_HD / 2), TC_V = TC_S + 2 * TA_NACC * TA_N, TC_O = TC_V + 2 * (TA_M / 2);
+static_assert(TC_O + 2 * TA_N <= TA_TMEM_COLS, "TMEM columns");
+constexpr int TA_PPART = TA_N * TA_M * 2;  // one bf16 part of p^T [16 head slots][128 rows]
 constexpr float TA_TAU = 8.0f;
 
 template <int KT>
@@ -54,14 +59,16 @@ struct TaGeom {
 
 constexpr size_t TA_OFF_RING = 0;                           // K slots, then V slots
 constexpr size_t TA_OFF_Q = TA_OFF_RING + TA_RING;
-constexpr size_t TA_OFF_P = TA_OFF_Q + 3 * TA_QPART;        // p [2 groups][128 rows][8 heads]
-constexpr size_t TA_OFF_RED = TA_OFF_P + 2 * TA_M * 8 * 4;  // merge: m, l, weights [3][8 warps][8]
-constexpr size_t TA_OFF_BAR = TA_OFF_RED + 3 * TA_RW * 8 * 4;
-constexpr size_t TA_OFF_TMEM = TA_OFF_BAR + 48 * 8;
+constexpr size_t TA_OFF_P = TA_OFF_Q + 3 * TA_QPART;  // p^T [2 groups][hi, lo][16][128] bf16
+// exchange of warp maxima [2 groups][2 tiles][4 warps][8], then the merge:
+// l [2 groups][4 warps][8], m [2][8], weights [2][8]
+constexpr size_t TA_OFF_RED = TA_OFF_P + 2 * 2 * TA_PPART;
+constexpr size_t TA_OFF_BAR = TA_OFF_RED + (2 * 2 * 4 * 8 + 2 * 4 * 8 + 2 * 8 + 2 * 8) * 4;
+constexpr size_t TA_OFF_TMEM = TA_OFF_BAR + 64 * 8;
 constexpr size_t TA_OFF_BT = TA_OFF_TMEM + 16;  // paged: the split's block-table entries
 constexpr size_t TA_SMEM = TA_OFF_BT + static_cast<size_t>(AT_BT_CACHE) * 4;
 static_assert(TA_SMEM <= 227 * 1024, "shared memory");
-static_assert(TA_RW * 8 * TA_HD * 4 <= TA_RING, "warp partials fit the rings");
+static_assert(2 * 8 * TA_HD * 4 <= TA_RING, "group partials fit the rings");
 
 __device__ __forceinline__ void ta_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile(
@@ -133,7 +140,7 @@ __device__ __forceinline__ void e4m3_unit_words(const uint4 raw, uint32_t *w) {
 template <int KT, int GT>
 __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
     using Geo = TaGeom<KT>;
-    constexpr int ES = Geo::ES, ROW = Geo::ROW, NST = Geo::NST;
+    constexpr int ROW = Geo::ROW, NST = Geo::NST;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t *kring = smem + TA_OFF_RING;
     uint8_t *vring = kring + static_cast<size_t>(NST) * Geo::SLOT;
@@ -141,7 +148,8 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
     float *red = reinterpret_cast<float *>(smem + TA_OFF_RED);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + TA_OFF_BAR);
     uint64_t *kfull = bars, *kempty = bars + NST, *vfull = bars + 2 * NST, *vempty = bars + 3 * NST;
-    uint64_t *kready = bars + 4 * NST, *sfull = kready + 2, *qready = sfull + 2;
+    uint64_t *kready = bars + 4 * NST, *sfull = kready + 2, *pvready = sfull + 2, *ofull = pvready + 2;
+    uint64_t *xch = ofull + 2, *qready = xch + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + TA_OFF_TMEM);
     int *bts = reinterpret_cast<int *>(smem + TA_OFF_BT);
 
@@ -209,6 +217,9 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(kready + i, 4);
             mbar_init(sfull + i, 1);
+            mbar_init(pvready + i, 4);
+            mbar_init(ofull + i, 1);
+            mbar_init(xch + i, 4);
         }
         mbar_init(qready, 4);
         fence_mbar_init();
@@ -285,16 +296,19 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
             if (!waited) pdl_wait();
         }
         __syncwarp();
-    } else if (warp == TA_RW + 1) {
-        // ---- MMA issue, tiles in order: S^T of tile k into group k % 2's S buffer
+    } else if (warp >= TA_RW + 1) {
+        // ---- MMA issue: warp 9 the scores of tiles 0, 1, ... (S(k) once the
+        // K rows of tile k are in TMEM), warp 10 the P V of tiles 0, 1, ...
+        // (once a tile's p and V^T are ready).  Each commits on its own
+        // barriers, so neither waits for the other's progress.
         if (lane == 0) {
             constexpr uint32_t IDS = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(TA_N >> 3) << 17) |
                                      (static_cast<uint32_t>(TA_M >> 4) << 24);
-            bool ok = mbar_wait(qready, 0);
             const uint64_t qd = ta_desc(sptr(qimg), TA_HD * 16);
-            for (int k = 0; k < ntiles && ok; ++k) {
+            const uint64_t pd0 = ta_desc(sptr(smem + TA_OFF_P), TA_M * 16);
+            auto issue_s = [&](int k) -> bool {
                 const int gi = k & 1;
-                if (!(ok = mbar_wait(kready + gi, (k >> 1) & 1))) break;
+                if (!mbar_wait(kready + gi, (k >> 1) & 1)) return false;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
                 for (int kq = 0; kq < TA_HD / 32; ++kq)  // k step within a half of the dims
@@ -316,6 +330,41 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
                 asm volatile(
                     "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sptr(sfull + gi))
                     : "memory");
+                return true;
+            };
+            auto issue_pv = [&](int k) -> bool {
+                constexpr uint32_t IDO = KT == KV_FP8 ? ((1u << 4) | (static_cast<uint32_t>(TA_N >> 3) << 17) |
+                                                          (static_cast<uint32_t>(TA_M >> 4) << 24))
+                                                       : IDS;
+                const int gi = k & 1;
+                if (!mbar_wait(pvready + gi, (k >> 1) & 1)) return false;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint64_t pd = pd0 + gi * (2 * TA_PPART / 16);
+#pragma unroll
+                for (int ks = 0; ks < TA_M / 16; ++ks)
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {  // p hi, p lo (V^T exact)
+                        const uint32_t at = taddr + TC_V + gi * (TA_M / 2) + ks * 8;
+                        const uint64_t bd = pd + part * (TA_PPART / 16) + ks * 16;
+                        const uint32_t acc = (k >= 2 || ks > 0 || part > 0) ? 1u : 0u;
+                        asm volatile(
+                            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+                                taddr + TC_O + gi * TA_N),
+                            "r"(at), "l"(bd), "r"(IDO), "r"(acc)
+                            : "memory");
+                    }
+                asm volatile(
+                    "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sptr(ofull + gi))
+                    : "memory");
+                return true;
+            };
+            bool ok = true;
+            if (warp == TA_RW + 1) {
+                ok = mbar_wait(qready, 0);
+                for (int k = 0; k < ntiles && ok; ++k) ok = issue_s(k);
+            } else {
+                for (int k = 0; k < ntiles && ok; ++k) ok = issue_pv(k);
             }
             if (!ok) flag_error(a.status, FLAG_TIMEOUT);
         }
@@ -324,7 +373,6 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
         // ---- rows: group gi takes tiles gi, gi + 2, ...; thread r = tile row = TMEM lane
         const int rw = warp - 1, gi = rw >> 2, wq = warp & 3, r = 32 * wq + lane;
         const uint32_t lanes = taddr + (static_cast<uint32_t>(32 * wq) << 16);
-        float *P = reinterpret_cast<float *>(smem + TA_OFF_P) + gi * TA_M * 8;  // [128 rows][8 heads]
         pdl_wait();  // q is the preceding grid's output
         if (gi == 0) {  // q of the group as three bf16 parts [16 head slots][128 dims], K-major core matrices
             const int h = r >> 3, d0 = (r & 7) * 16;
@@ -407,16 +455,21 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
             return true;
         };
 
+        uint8_t *pt = smem + TA_OFF_P + static_cast<size_t>(gi) * 2 * TA_PPART;  // p^T hi, lo of this group
+        float *xr = red;                                   // [2 groups][2 tiles][4 warps][8]
+        float *lr = red + 2 * 2 * 4 * 8;                   // [2 groups][4 warps][8]
+        float *mg = lr + 2 * 4 * 8, *wg = mg + 2 * 8;      // [2 groups][8]
+        for (int i = r; i < 2 * TA_PPART / 4; i += 128) reinterpret_cast<uint32_t *>(pt)[i] = 0u;  // head slots >= GT stay 0
+        asm volatile("bar.sync 3, 256;" ::: "memory");
         float m[GT], lp[GT], al[GT];
-        float2 acc[GT][2];  // dims 4 lane .. 4 lane + 3 of each head slot
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
             m[j] = -INFINITY;
             lp[j] = 0.0f;
-            acc[j][0] = acc[j][1] = make_float2(0.0f, 0.0f);
         }
         bool ok = gi < ntiles ? store_k(gi) : true;
-        for (int k = gi, j2 = 0; k < ntiles && ok; k += 2, ++j2) {
+        int j2 = 0;
+        for (int k = gi; k < ntiles && ok; k += 2, ++j2) {
             const int sl = k % NST;
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(sfull + gi, j2 & 1)))) break;
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -439,115 +492,141 @@ __global__ void __launch_bounds__(TA_THREADS, 1) k_attn_tc(const AttnArgs a) {
             // this tile's scores are in registers: the next tile's K rows may
             // replace the K buffer (its MMAs also overwrite the S buffer)
             if (k + 2 < ntiles && !(ok = store_k(k + 2))) break;
-            // this warp's rows: the tile maximum of each head
+            // the tile maximum of each head over the group's 128 rows
+            float *xw = xr + ((gi * 2 + (j2 & 1)) * 4) * 8;
 #pragma unroll
             for (int j = 0; j < GT; ++j) {
-                const float tm = warp_max(sc[j]);
+                const float wm = warp_max(sc[j]);
+                if (lane == 0) xw[wq * 8 + j] = wm;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xch + gi);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(xch + gi, j2 & 1)))) break;
+            bool rescale = false;
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                const float tm = fmaxf(fmaxf(xw[j], xw[8 + j]), fmaxf(xw[16 + j], xw[24 + j]));
                 al[j] = 1.0f;
-                if (tm > m[j] + TA_TAU) {  // the same decision in every lane of the warp
+                if (tm > m[j] + TA_TAU) {  // the same decision in every thread of the group
                     al[j] = exp2f(m[j] - tm);
                     m[j] = tm;
+                    rescale = j2 > 0;
                 }
-                const float p = sc[j] == -INFINITY ? 0.0f : exp2f(sc[j] - m[j]);
-                lp[j] = lp[j] * al[j] + p;
-                sc[j] = p;
-                acc[j][0] = __fmul2_rn(acc[j][0], make_float2(al[j], al[j]));
-                acc[j][1] = __fmul2_rn(acc[j][1], make_float2(al[j], al[j]));
+                const float pj = sc[j] == -INFINITY ? 0.0f : exp2f(sc[j] - m[j]);
+                lp[j] = lp[j] * al[j] + pj;
+                sc[j] = pj;
             }
-            {
-                float pw[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) pw[j] = 0.0f;
-#pragma unroll
-                for (int j = 0; j < GT; ++j) pw[j] = sc[j];
-                *reinterpret_cast<float4 *>(P + r * 8) = make_float4(pw[0], pw[1], pw[2], pw[3]);
-                *reinterpret_cast<float4 *>(P + r * 8 + 4) = make_float4(pw[4], pw[5], pw[6], pw[7]);
+            // the group's previous P.V is done: O^T is stable, V^T and p^T are free
+            if (j2 > 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(ofull + gi, (j2 - 1) & 1)))) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             }
-            __syncwarp();
-            // O += P V over this warp's 32 rows of the tile
+            if (rescale) {  // uniform in the group; this thread's lane = dim r of O^T
+                uint32_t v[16];
+                ta_ld16(lanes + TC_O + gi * TA_N, v);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int j = 0; j < GT; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * al[j]);
+                ta_st16(lanes + TC_O + gi * TA_N, v);
+            }
+            // V^T: this thread's lane takes dim r of the tile's rows (zeros past n)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(vfull + sl, (k / NST) & 1)))) break;
-            const uint8_t *vt = vring + static_cast<size_t>(sl) * Geo::SLOT;
-            const int rb = 32 * wq, re = min(n, rb + 32);
-            int rr = rb;
-            for (; rr + 4 <= re; rr += 4) {  // four rows: every load issued before the FMAs
-                float4 pa[4], pb[4], v[4];
+            {
+                const uint8_t *vt = vring + static_cast<size_t>(sl) * Geo::SLOT;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    pa[u] = *reinterpret_cast<const float4 *>(P + (rr + u) * 8);
-                    pb[u] = *reinterpret_cast<const float4 *>(P + (rr + u) * 8 + 4);
-                    v[u] = kv_load4<KT>(vt + (static_cast<size_t>(rr + u) * TA_HD + 4 * lane) * ES);
-                }
+                for (int c = 0; c < TA_M / 32; ++c) {  // 32 rows = 16 columns per store
+                    uint32_t w[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float pv[8] = {pa[u].x, pa[u].y, pa[u].z, pa[u].w, pb[u].x, pb[u].y, pb[u].z, pb[u].w};
-                    const float2 v01 = make_float2(v[u].x, v[u].y), v23 = make_float2(v[u].z, v[u].w);
-#pragma unroll
-                    for (int j = 0; j < GT; ++j) {
-                        const float2 pp = make_float2(pv[j], pv[j]);
-                        acc[j][0] = __ffma2_rn(pp, v01, acc[j][0]);
-                        acc[j][1] = __ffma2_rn(pp, v23, acc[j][1]);
+                    for (int i = 0; i < 16; ++i) {
+                        const int k0 = 32 * c + 2 * i;
+                        if constexpr (KT == KV_BF16) {
+                            const uint32_t lo = k0 < n ? *reinterpret_cast<const uint16_t *>(vt + (k0 * TA_HD + r) * 2) : 0u;
+                            const uint32_t hi =
+                                k0 + 1 < n ? *reinterpret_cast<const uint16_t *>(vt + ((k0 + 1) * TA_HD + r) * 2) : 0u;
+                            w[i] = lo | (hi << 16);
+                        } else {  // two E4M3 codes -> an exact f16 pair
+                            const uint32_t lo = k0 < n ? vt[k0 * TA_HD + r] : 0u;
+                            const uint32_t hi = k0 + 1 < n ? vt[(k0 + 1) * TA_HD + r] : 0u;
+                            uint32_t h2;
+                            asm("cvt.rn.f16x2.e4m3x2 %0, %1;"
+                                : "=r"(h2)
+                                : "h"(static_cast<unsigned short>(lo | (hi << 8))));
+                            w[i] = h2;
+                        }
                     }
-                }
-            }
-            for (; rr < re; ++rr) {
-                const float4 pa = *reinterpret_cast<const float4 *>(P + rr * 8);
-                const float4 pb = *reinterpret_cast<const float4 *>(P + rr * 8 + 4);
-                const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
-                const float4 v = kv_load4<KT>(vt + (static_cast<size_t>(rr) * TA_HD + 4 * lane) * ES);
-                const float2 v01 = make_float2(v.x, v.y), v23 = make_float2(v.z, v.w);
-#pragma unroll
-                for (int j = 0; j < GT; ++j) {
-                    const float2 pp = make_float2(pv[j], pv[j]);
-                    acc[j][0] = __ffma2_rn(pp, v01, acc[j][0]);
-                    acc[j][1] = __ffma2_rn(pp, v23, acc[j][1]);
+                    ta_st16(lanes + TC_V + gi * (TA_M / 2) + 16 * c, w);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(vempty + sl);
+            if (lane == 0) mbar_arrive(vempty + sl);  // the V rows are in TMEM
+            // p^T: row r's probabilities as hi and lo parts (bf16, or f16 for
+            // fp8 caches; p <= 2^8 fits f16), K-major [head slot][row]
+#pragma unroll
+            for (int j = 0; j < GT; ++j) {
+                const int off = (j >> 3) * (TA_M * 16) + (r >> 3) * 128 + (j & 7) * 16 + (r & 7) * 2;
+                if constexpr (KT == KV_FP8) {
+                    const __half ph = __float2half_rn(sc[j]);
+                    *reinterpret_cast<__half *>(pt + off) = ph;
+                    *reinterpret_cast<__half *>(pt + TA_PPART + off) = __float2half_rn(sc[j] - __half2float(ph));
+                } else {
+                    const __nv_bfloat16 ph = __float2bfloat16_rn(sc[j]);
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + off) = ph;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + TA_PPART + off) =
+                        __float2bfloat16_rn(sc[j] - __bfloat162float(ph));
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pvready + gi);
         }
+        const int ntile_g = ntiles > gi ? (ntiles - gi + 1) / 2 : 0;  // this group's tiles
+        if (ok && ntile_g > 0) ok = __all_sync(0xffffffffu, mbar_wait(ofull + gi, (ntile_g - 1) & 1));
         if (!ok) flag_error(a.status, FLAG_TIMEOUT);
-        // ---- the split's record: the eight warps' states merged with
-        // weights exp2(m_w - M) per head
-        asm volatile("bar.sync 2, 256;" ::: "memory");  // every tile consumed: the rings are idle
-        float *mw = red;                  // [8][8] running maxima
-        float *lw = red + TA_RW * 8;      // [8][8] row sums
-        float *ww = red + 2 * TA_RW * 8;  // [8][8] weights
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        // ---- the split's record: the two groups' states merged with weights
+        // exp2(m_g - M) per head.  After both groups have left their loops
+        // the rings are idle (every copy consumed, every MMA done).
+        asm volatile("bar.sync 3, 256;" ::: "memory");
+        float *accg = reinterpret_cast<float *>(kring);  // [2 groups][8 heads][128 dims]
+        {
+            uint32_t v[16];
+            ta_ld16(lanes + TC_O + gi * TA_N, v);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < GT; ++j)
+                accg[(gi * 8 + j) * TA_HD + r] = (ok && ntile_g > 0) ? __uint_as_float(v[j]) : 0.0f;
+        }
 #pragma unroll
         for (int j = 0; j < GT; ++j) {
             const float ls = warp_sum(lp[j]);
-            if (lane == 0) {
-                mw[rw * 8 + j] = m[j];
-                lw[rw * 8 + j] = ls;
-            }
+            if (lane == 0) lr[(gi * 4 + wq) * 8 + j] = ls;
         }
-        float *accw = reinterpret_cast<float *>(kring);  // [8 warps][8 heads][128]
 #pragma unroll
         for (int j = 0; j < GT; ++j)
-            *reinterpret_cast<float4 *>(accw + (rw * 8 + j) * TA_HD + 4 * lane) =
-                make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y);
-        asm volatile("bar.sync 2, 256;" ::: "memory");
-        const int ct = 32 * rw + lane;
+            if (r == j) mg[gi * 8 + j] = ntile_g > 0 ? m[j] : -INFINITY;
+        asm volatile("bar.sync 3, 256;" ::: "memory");
+        const int ct = 128 * gi + r;
         if (ct < G) {
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < TA_RW; ++w) M = fmaxf(M, mw[w * 8 + ct]);
+            const float M = fmaxf(mg[ct], mg[8 + ct]);
             float Ls = 0.0f;
 #pragma unroll
-            for (int w = 0; w < TA_RW; ++w) {
-                const float mv = mw[w * 8 + ct];
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const float mv = mg[g2 * 8 + ct];
                 const float sw = mv != -INFINITY ? exp2f(mv - M) : 0.0f;
-                ww[w * 8 + ct] = sw;
-                Ls = fmaf(sw, lw[w * 8 + ct], Ls);
+                wg[g2 * 8 + ct] = sw;
+                const float lsum = lr[(g2 * 4) * 8 + ct] + lr[(g2 * 4 + 1) * 8 + ct] + lr[(g2 * 4 + 2) * 8 + ct] +
+                                   lr[(g2 * 4 + 3) * 8 + ct];
+                Ls = fmaf(sw, lsum, Ls);
             }
             rec[ct] = M;
             rec[G + ct] = Ls;
         }
-        asm volatile("bar.sync 2, 256;" ::: "memory");
-        for (int idx = ct; idx < G * TA_HD; idx += 32 * TA_RW) {
+        asm volatile("bar.sync 3, 256;" ::: "memory");
+        for (int idx = ct; idx < G * TA_HD; idx += 256) {
             const int jj = idx / TA_HD, d = idx - jj * TA_HD;
-            float t = 0.0f;
-#pragma unroll
-            for (int w = 0; w < TA_RW; ++w) t = fmaf(ww[w * 8 + jj], accw[(w * 8 + jj) * TA_HD + d], t);
+            float t = fmaf(wg[jj], accg[jj * TA_HD + d], wg[8 + jj] * accg[(8 + jj) * TA_HD + d]);
             if constexpr (KT == KV_FP8) t *= a.v_scale;
             rec[2 * G + idx] = t;
         }
