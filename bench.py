@@ -153,15 +153,16 @@ def launches_per_layer(w) -> int:
     return 4 if (w.D // 32) % 8 == 0 else 5
 
 
-def profiled_traffic(kernel: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the kernel source as it is now (same hash); else None."""
+def profiled_traffic(key: str, source: str):
+    """DRAM bytes per launch of kernel@workload `key` from a committed ncu
+    summary, if it was taken on the kernel source as it is now (same hash);
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         src = open(os.path.join(ROOT, source), "rb").read()
-        entry = d.get(kernel)
+        entry = d.get(key)
         if entry and entry.get("source_sha256") == hashlib.sha256(src).hexdigest():
             return entry.get("dram_bytes_per_launch")
     except (OSError, ValueError):
@@ -361,7 +362,7 @@ def run_ours(args, ws, rank, local, pg):
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
                      "bytes_per_launch": att_bytes, "ms_per_launch": round(att_ms, 6),
-                     "traffic": profiled_traffic("k_attn_split",
+                     "traffic": profiled_traffic(f"k_attn_split@{args.config}",
                                                  "quantized_weight_attention_gb300/csrc/ck_attn_kernels.cuh")},
         "e2e": {"value": round(e2e_value, 1), "unit": "layer-steps/s", "h2d_bytes_per_step": w.D * 4,
                 "d2h_bytes_per_step": w.D * 4, "steps": Ke,
@@ -568,7 +569,12 @@ def run_attn_kv(args, ws, pg, torch, q, synth, dev):
             "step_hbm_gbs": round(ach, 1), "step_bytes": kv_bytes,
             "roofline": {"kernel": "attention (split + combine, one call)", "bound": "hbm", "achieved": round(ach, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                         "peak_kind": f"{peak_kind} hbm_gbs", "traffic": None},
+                         "peak_kind": f"{peak_kind} hbm_gbs",
+                         "traffic": profiled_traffic(
+                             (f"k_attn_split@attn{Tn}_{dt}" if dt == "f32" else f"k_attn_tc@attn{Tn}_{dt}")
+                             + ("" if S < 0 else f"_s{S}"),
+                             "quantized_weight_attention_gb300/csrc/" +
+                             ("ck_attn_kernels.cuh" if dt == "f32" else "ck_attn_tc.cu"))},
             "e2e": {"value": round(ws * Ke / (e2e_ms / 1e3), 1), "unit": "attention-calls/s",
                     "h2d_bytes_per_step": H * hd * 4, "d2h_bytes_per_step": H * hd * 4, "steps": Ke,
                     "how": "per call: pinned q -> device, the attention call, out -> pinned host"},
@@ -916,7 +922,8 @@ def run_prefill(args, ws, pg, torch, q, synth, dev):
                          "frac": round(attn_tf / bf16_peak, 4),
                          "peak_kind": f"{bf16_kind}; the split-precision operands take 3 bf16 MMAs per product, "
                                       f"so this kernel's algorithmic ceiling is 1/3 of the peak",
-                         "traffic": None},
+                         "traffic": profiled_traffic("k_pf_attn@prefill512",
+                                                     "quantized_weight_attention_gb300/csrc/ck_prefill_attn.cu")},
             "e2e": {"value": round(ws * n * Ke / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": n * w.D * 4, "d2h_bytes_per_step": n * w.D * 4, "steps": Ke,
                     "how": "per step: pinned x [n, D] -> device, ck_prefill_layer, out -> pinned host"},

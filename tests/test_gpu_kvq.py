@@ -89,6 +89,9 @@ CASES = [
     (128, 32, 4, 8193, 8256),   # G = 8, the 8K length
     (64, 16, 2, 20011, 20016),  # long splits of a head_dim 64 cache
     (128, 28, 4, 32769, 32832), # 32K rows: large stages
+    (128, 4, 4, 129, 192),      # G = 1: a full 128-row tile and a one-row tile
+    (128, 8, 4, 257, 320),      # G = 2: three tiles, the two row groups unevenly loaded
+    (128, 16, 2, 128, 128),     # G = 8: exactly one tile, the cache full
 ]
 
 
@@ -102,6 +105,10 @@ def test_attention_kvq_matches_oracle(dev, kind, hd, Hq, KV, Tn, C):
     ks = float(np.abs(k).max() / 448.0 * 1.01)
     vs = float(np.abs(v).max() / 448.0 * 1.01)
     kc, vc = encode(kind, k, ks), encode(kind, v, vs)
+    # rows past the attended ones hold NaN codes: they must never be read
+    nan = 0x7FC0 if kind == oracle.KV_BF16 else 0x7F
+    kc[:, Tn:] = nan
+    vc[:, Tn:] = nan
     ref = oracle.attention_kvq(qv, kc, vc, Hq, KV, Tn, C, hd, kind, ks, vs)
     nbytes = q.ck_attn_scratch_size(Hq, KV, C, hd)
     scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)

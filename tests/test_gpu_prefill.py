@@ -258,10 +258,11 @@ def test_prefill_tensor_core_attention_shapes(dev, D, H, KV, pos, n, C):
 
 
 @pytest.mark.parametrize("H,KV,pos,n,C", [(28, 4, 0, 1, 64), (28, 4, 130, 33, 200), (16, 2, 7000, 300, 7300),
-                                          (8, 8, 10, 70, 96), (32, 2, 64, 64, 128)])
+                                          (8, 8, 10, 70, 96), (32, 2, 64, 64, 128), (28, 4, 0, 1024, 1024)])
 def test_attn_prefill_alone(dev, H, KV, pos, n, C):
     """ck_attn_prefill_gqa against the oracle's decode attention over pos + i + 1
-    rows for every token (groups of 7, 8, 1 and 16; a 7,300-row cache)."""
+    rows for sampled tokens (groups of 7, 8, 1 and 16; a 7,300-row cache; a
+    1,024-token chunk from an empty cache filling it: 256 CTAs)."""
     hd = 128
     rng = np.random.default_rng(pos + n + H)
     kc0 = rng.standard_normal((KV, C, hd)).astype(np.float32)
