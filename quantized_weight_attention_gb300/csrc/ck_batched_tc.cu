@@ -313,6 +313,11 @@ __global__ void __launch_bounds__(TW_THREADS, 1) k_proj_tc(const BatchArgs a, in
         copy_b(0);
         for (int t = 0; t < T; ++t) {
             const int i = t % TW_NA;
+            if (t + 3 < T) {  // three stages ahead into L1: the loads below then hit close by
+                const uint8_t *pf = wrow + static_cast<size_t>(k0 + t + 3) * (TP_BPS / 2) * pb;
+                prefetch_l1(pf);
+                prefetch_l1(pf + 4 * TP_PAIR_WORDS - 1);
+            }
             if (t + 1 < T) {
                 load_pair(wrow + static_cast<size_t>(k0 + t + 1) * (TP_BPS / 2) * pb, wq8, rn);
                 // slot (t + 1) % TW_NA is free once stage t + 1 - TW_NA is read back

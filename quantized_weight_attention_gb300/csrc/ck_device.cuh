@@ -109,6 +109,11 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
 // Programmatic dependent launch: wait until the preceding grid in the
 // stream has completed and its writes are visible (no-op without PDL) /
 // allow the following grid to begin launching.
+// Bring the cache line holding `p` into L1 (no register result).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
