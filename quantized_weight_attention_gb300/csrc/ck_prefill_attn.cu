@@ -68,12 +68,12 @@ __device__ __forceinline__ uint64_t pf_desc(uint32_t saddr, uint32_t sbo) {
 __device__ __forceinline__ void bf_split8(const float (&x)[8], uint4 &hi, uint4 &lo) {
     uint32_t h[4], l[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat16 a = __float2bfloat16_rn(x[2 * i]), b = __float2bfloat16_rn(x[2 * i + 1]);
-        const __nv_bfloat16 la = __float2bfloat16_rn(x[2 * i] - __bfloat162float(a));
-        const __nv_bfloat16 lb = __float2bfloat16_rn(x[2 * i + 1] - __bfloat162float(b));
-        h[i] = static_cast<uint32_t>(__bfloat16_as_ushort(a)) | (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
-        l[i] = static_cast<uint32_t>(__bfloat16_as_ushort(la)) | (static_cast<uint32_t>(__bfloat16_as_ushort(lb)) << 16);
+    for (int i = 0; i < 4; ++i) {  // packed conversions, two values each
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        const float2 hf = __bfloat1622float2(hb);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(x[2 * i] - hf.x, x[2 * i + 1] - hf.y);
+        h[i] = *reinterpret_cast<const uint32_t *>(&hb);
+        l[i] = *reinterpret_cast<const uint32_t *>(&lb);
     }
     hi = make_uint4(h[0], h[1], h[2], h[3]);
     lo = make_uint4(l[0], l[1], l[2], l[3]);
@@ -269,13 +269,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
                     for (int i = 0; i < 16; ++i) p[16 * c + i] = __uint_as_float(v[c][i]);
             }
             const int k0 = j * PF_N;
-            float mt = -INFINITY;
+            // the causal mask only where a row of this tile may end inside the
+            // key tile (the same for the whole CTA: its first token's limit)
+            if (k0 + PF_N - 1 > a.pos + tl0) {
 #pragma unroll
-            for (int c = 0; c < PF_N; ++c) {
-                const float s = k0 + c <= limit ? p[c] * a.scale_log2 : -INFINITY;
-                p[c] = s;
-                mt = fmaxf(mt, s);
+                for (int c = 0; c < PF_N; ++c)
+                    if (k0 + c > limit) p[c] = -INFINITY;
             }
+            // maximum on the raw scores (the scale is positive), then one FMA per exp2
+            float mr = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < PF_N; ++c) mr = fmaxf(mr, p[c]);
+            const float mt = mr * a.scale_log2;
             float alpha = 1.0f;
             bool rescale = false;
             if (mt > m + PF_TAU) {
@@ -285,9 +290,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
                 m = mt;
             }
             float ps = 0.0f;
+            const float nm = -m;
 #pragma unroll
             for (int c = 0; c < PF_N; ++c) {
-                p[c] = exp2f(p[c] - m);
+                p[c] = exp2f(fmaf(p[c], a.scale_log2, nm));
                 ps += p[c];
             }
             l += ps;
