@@ -80,13 +80,16 @@ def dist_setup():
 def barrier(pg, torch):
     if pg is not None:
         pg.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(pg, torch, v: float) -> float:
+    """The largest of the ranks' values (the slowest rank's time)."""
     if pg is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.cuda.is_available() and pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
 
