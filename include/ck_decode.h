@@ -152,7 +152,12 @@ int ck_attn_decode_gqa_noalloc(const float *q, const float *k_cache, const float
  *     no infinities): the value is code * k_scale (keys), code * v_scale
  *     (values); k_scale, v_scale finite and > 0 (else CK_EINVAL).
  * head_dim in {64, 128} (else CK_EINVAL); otherwise the arguments,
- * requirements, scratch and result of ck_attn_decode_gqa. */
+ * requirements, scratch and result of ck_attn_decode_gqa.  Arithmetic: at
+ * head_dim 128 both products run on the tensor cores with fp32
+ * accumulation.  The cache values are exact there, q is taken as three
+ * bf16 parts (scores to fp32 quality), and the probabilities as two parts
+ * (bf16 for bf16 caches, fp16 for fp8), about 2^-17 / 2^-22 relative.  At
+ * head_dim 64 the arithmetic is fp32 on the CUDA cores. */
 int ck_attn_decode_gqa_bf16(const float *q, const void *k_cache, const void *v_cache, float *out, int num_heads,
                             int num_kv_heads, int kv_tokens, int cache_capacity, int head_dim, void *scratch,
                             size_t scratch_bytes, void *stream);
