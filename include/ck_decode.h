@@ -370,6 +370,18 @@ int ck_prefill_layer(float *out, const float *x, const float *residual, const vo
                      const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
                      const float *rope_sin, int pos, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
                      int head_dim, int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream);
+/* The same with the chunk's first position read on the device from d_pos
+ * (int32, device memory set before the call's first kernel), for replaying a
+ * captured graph as the chunk moves.  A chunk that does not fit the cache
+ * (*d_pos < 0 or *d_pos + n_tokens > cache_capacity) writes nothing (no
+ * cache row, no output) and raises CK_ERANGE in the device status word
+ * (ck_device_status).  d_pos null: CK_EINVAL. */
+int ck_prefill_layer_devpos(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                            const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                            const float *rope_sin, const int32_t *d_pos, int n_tokens, int embed_dim, int num_heads,
+                            int num_kv_heads, int head_dim, int cache_capacity, float eps, void *scratch,
+                            size_t scratch_bytes, void *stream);
 
 /* ---- test access to the integer block dots ----------------------------- */
 

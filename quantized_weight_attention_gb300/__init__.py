@@ -23,6 +23,7 @@ __all__ = [
     "lib", "check", "ck_status_string", "ck_quantize_q8_0", "ck_gemv_q5_0_q8_0", "ck_gemv_q8_0_q8_0",
     "ck_rope_inplace", "ck_kv_store", "ck_attn_scratch_size", "ck_attn_decode_gqa",
     "ck_prefill_layer_scratch_size", "ck_prefill_layer_scratch_offset", "ck_prefill_layer",
+    "ck_prefill_layer_devpos",
     "ck_attn_split_scratch_size", "ck_attn_decode_gqa_split",
     "ck_attn_prefill_scratch_size", "ck_attn_prefill_gqa",
     "ck_decode_layer_scratch_size", "ck_decode_layer", "ck_decode_layer_devpos", "ck_device_status",
@@ -76,6 +77,7 @@ _SIGS = {
     "ck_prefill_layer_scratch_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "ck_prefill_layer_scratch_offset": (_SZ, [_I, _I, _I, _I, _I, _I, _I]),
     "ck_prefill_layer": (_I, [_P] * 16 + [_I] * 7 + [_F, _P, _SZ, _P]),
+    "ck_prefill_layer_devpos": (_I, [_P] * 17 + [_I] * 6 + [_F, _P, _SZ, _P]),
     "ck_attn_split_scratch_size": (_SZ, [_I, _I, _I, _I]),
     "ck_attn_prefill_scratch_size": (_SZ, [_I, _I, _I, _I]),
     "ck_attn_prefill_gqa": (_I, [_P] * 4 + [_I] * 6 + [_P, _SZ, _P]),
@@ -281,6 +283,18 @@ def ck_decode_layer_batched_scratch_offset(tap: int, batch: int, embed_dim: int,
                                            head_dim: int, cache_capacity: int) -> int:
     return lib().ck_decode_layer_batched_scratch_offset(tap, batch, embed_dim, num_heads, num_kv_heads, head_dim,
                                                         cache_capacity)
+
+
+def ck_prefill_layer_devpos(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
+                            rope_sin, d_pos, n_tokens: int, embed_dim: int, num_heads: int, num_kv_heads: int,
+                            head_dim: int, cache_capacity: int, eps: float, scratch, scratch_bytes: int,
+                            stream=None) -> int:
+    """ck_prefill_layer with the chunk's first position in device memory (int32 tensor)."""
+    return lib().ck_prefill_layer_devpos(
+        _ptr(out), _ptr(x), _ptr(residual), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(wo), _ptr(gamma), _ptr(bq), _ptr(bk),
+        _ptr(bv), _ptr(bo), _ptr(k_cache), _ptr(v_cache), _ptr(rope_cos), _ptr(rope_sin), _ptr(d_pos), n_tokens,
+        embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps, _ptr(scratch), scratch_bytes,
+        _stream(stream))
 
 
 def ck_attn_prefill_scratch_size(num_heads: int, num_kv_heads: int, head_dim: int, cache_capacity: int) -> int:

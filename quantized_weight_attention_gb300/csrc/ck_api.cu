@@ -576,7 +576,8 @@ static int batched_body(float *out, const float *x, const float *residual, const
                         const float *rope_cos, const float *rope_sin, const int32_t *d_pos, int batch, int embed_dim,
                         int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps, uint8_t *sc,
                         const BatchScratch &L, cudaStream_t s, bool pdl_first, int chunk_pos,
-                        uint8_t *pf_img = nullptr, float *pf_k = nullptr, float *pf_v = nullptr) {
+                        uint8_t *pf_img = nullptr, float *pf_k = nullptr, float *pf_v = nullptr,
+                        const int32_t *pf_dpos = nullptr) {
     unsigned *st = status_word();
     if (!st) return CK_ECUDA;
 
@@ -648,7 +649,7 @@ static int batched_body(float *out, const float *x, const float *residual, const
     aa.l2_prefetch_bytes = static_cast<size_t>(embed_dim) * (num_heads * head_dim / 32) * 22;
     aa.status = st;
     if (pf_img) {  // a prefill chunk on the tensor cores
-        if (launch_prefill_attn(aa, ba.q, pf_k, pf_v, pf_img, batch, chunk_pos, num_heads, num_kv_heads,
+        if (launch_prefill_attn(aa, ba.q, pf_k, pf_v, pf_img, batch, chunk_pos, pf_dpos, num_heads, num_kv_heads,
                                 cache_capacity, s))
             return CK_ECUDA;
     } else if (launch_attention(aa, batch, s, true, true)) {
@@ -744,22 +745,23 @@ int ck_attn_prefill_gqa(const float *q, const float *k_cache, const float *v_cac
     o.hd = head_dim;
     o.out = out;
     o.status = st;
-    return launch_prefill_attn(o, q, k_cache, v_cache, static_cast<uint8_t *>(scratch), n_tokens, pos, num_heads,
-                               num_kv_heads, cache_capacity, as_stream(stream))
+    return launch_prefill_attn(o, q, k_cache, v_cache, static_cast<uint8_t *>(scratch), n_tokens, pos, nullptr,
+                               num_heads, num_kv_heads, cache_capacity, as_stream(stream))
                ? CK_ECUDA
                : CK_OK;
 }
 
-int ck_prefill_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
-                     const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
-                     const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
-                     const float *rope_sin, int pos, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
-                     int head_dim, int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream) {
+static int prefill_common(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                          const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                          const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                          const float *rope_sin, int pos, const int32_t *d_pos, int n_tokens, int embed_dim,
+                          int num_heads, int num_kv_heads, int head_dim, int cache_capacity, float eps, void *scratch,
+                          size_t scratch_bytes, void *stream) {
     int rc = check_ptrs({out, x, residual, wq, wk, wv, wo, gamma, k_cache, v_cache, rope_cos, rope_sin},
-                        {bq, bk, bv, bo});
+                        {bq, bk, bv, bo, d_pos});
     if (rc) return rc;
     if ((rc = batch_shape_check(n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity))) return rc;
-    if (pos < 0 || pos > cache_capacity - n_tokens) return CK_ERANGE;
+    if (!d_pos && (pos < 0 || pos > cache_capacity - n_tokens)) return CK_ERANGE;
     if (!aligned16(k_cache) || !aligned16(v_cache)) return CK_EALIGN;
     if (!scratch) return CK_ESCRATCH;
     if (!aligned16(scratch)) return CK_EALIGN;
@@ -768,14 +770,42 @@ int ck_prefill_layer(float *out, const float *x, const float *residual, const vo
     if (out == x || out == residual) return CK_EINVAL;
     uint8_t *sc = static_cast<uint8_t *>(scratch);
     cudaStream_t s = as_stream(stream);
+    unsigned *st = status_word();
+    if (!st) return CK_ECUDA;
     float **kcs = reinterpret_cast<float **>(sc + P.off_kcs);
     float **vcs = reinterpret_cast<float **>(sc + P.off_vcs);
     int32_t *pos_of = reinterpret_cast<int32_t *>(sc + P.off_pos);
-    if (launch_prefill_setup(kcs, vcs, pos_of, k_cache, v_cache, pos, n_tokens, s)) return CK_ECUDA;
-    // the first batched launch waits for the whole setup grid (no overlap)
+    if (launch_prefill_setup(kcs, vcs, pos_of, k_cache, v_cache, pos, d_pos, n_tokens, cache_capacity, st, s))
+        return CK_ECUDA;
+    // The first batched launch waits for the whole setup grid (no overlap).
+    // With the position on the device the decode-path attention treats every
+    // row as possibly new (chunk start 0).
     return batched_body(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, kcs, vcs, rope_cos, rope_sin,
                         pos_of, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity, eps, sc,
-                        P.b, s, false, pos, P.tc_attn ? sc + P.off_img : nullptr, k_cache, v_cache);
+                        P.b, s, false, d_pos ? 0 : pos, P.tc_attn ? sc + P.off_img : nullptr, k_cache, v_cache,
+                        d_pos);
+}
+
+int ck_prefill_layer(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                     const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                     const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                     const float *rope_sin, int pos, int n_tokens, int embed_dim, int num_heads, int num_kv_heads,
+                     int head_dim, int cache_capacity, float eps, void *scratch, size_t scratch_bytes, void *stream) {
+    return prefill_common(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
+                          rope_sin, pos, nullptr, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim,
+                          cache_capacity, eps, scratch, scratch_bytes, stream);
+}
+
+int ck_prefill_layer_devpos(float *out, const float *x, const float *residual, const void *wq, const void *wk,
+                            const void *wv, const void *wo, const float *gamma, const float *bq, const float *bk,
+                            const float *bv, const float *bo, float *k_cache, float *v_cache, const float *rope_cos,
+                            const float *rope_sin, const int32_t *d_pos, int n_tokens, int embed_dim, int num_heads,
+                            int num_kv_heads, int head_dim, int cache_capacity, float eps, void *scratch,
+                            size_t scratch_bytes, void *stream) {
+    if (!d_pos) return CK_EINVAL;
+    return prefill_common(out, x, residual, wq, wk, wv, wo, gamma, bq, bk, bv, bo, k_cache, v_cache, rope_cos,
+                          rope_sin, 0, d_pos, n_tokens, embed_dim, num_heads, num_kv_heads, head_dim, cache_capacity,
+                          eps, scratch, scratch_bytes, stream);
 }
 
 size_t ck_decode_layer_scratch_offset(int tap, int embed_dim, int num_heads, int num_kv_heads, int head_dim,

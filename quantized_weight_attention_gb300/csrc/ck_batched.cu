@@ -229,18 +229,21 @@ bool batched_shape_ok(int D, int H, int hd) {
 // The multi-token (prefill) form runs as a batch whose entries are the chunk's
 // tokens: every entry names the one cache, entry i sits at position pos + i.
 __global__ void k_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos,
-                                int n) {
+                                const int32_t *d_pos, int n, int C, unsigned *status) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int p0 = d_pos ? *d_pos : pos;
+    const bool fits = p0 >= 0 && p0 <= C - n;
+    if (!fits && i == 0) flag_error(status, FLAG_RANGE);
     if (i < n) {
         kcs[i] = k_cache;
         vcs[i] = v_cache;
-        pos_of[i] = pos + i;
+        pos_of[i] = fits ? p0 + i : C;
     }
 }
 
-int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos, int n,
-                         cudaStream_t s) {
-    void *args[] = {&kcs, &vcs, &pos_of, &k_cache, &v_cache, &pos, &n};
+int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos,
+                         const int32_t *d_pos, int n, int C, unsigned *status, cudaStream_t s) {
+    void *args[] = {&kcs, &vcs, &pos_of, &k_cache, &v_cache, &pos, &d_pos, &n, &C, &status};
     return launch(reinterpret_cast<const void *>(k_prefill_setup), dim3((n + 255) / 256), dim3(256), 0, s, false,
                   args) == cudaSuccess
                ? 0

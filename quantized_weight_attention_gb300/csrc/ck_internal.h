@@ -102,8 +102,12 @@ struct TpPlan {
 TpPlan tp_plan(int B, int D, int H, int KV, int hd, bool with_device);
 int launch_rows_tc(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 int launch_norm_pack(const BatchArgs &a, cudaStream_t s, bool pdl);
-int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos, int n,
-                         cudaStream_t s);
+// Per-token cache pointers and positions of a prefill chunk (token i at
+// pos + i, pos read from d_pos when it is not null); a chunk that does not
+// fit the cache gets every position at C (each kernel then skips the token)
+// and raises CK_ERANGE in the status word.
+int launch_prefill_setup(float **kcs, float **vcs, int32_t *pos_of, float *k_cache, float *v_cache, int pos,
+                         const int32_t *d_pos, int n, int C, unsigned *status, cudaStream_t s);
 int launch_rows_batched(const BatchArgs &a, bool oproj, cudaStream_t s, bool pdl);
 void plan_qkv(QkvArgs &a);
 
@@ -158,7 +162,7 @@ int launch_attention_tc(const AttnArgs &a, int B, cudaStream_t s, bool pdl_first
 bool prefill_tc_ok(int H, int KV, int hd);
 size_t prefill_img_bytes(int KV, int C);
 int launch_prefill_attn(const AttnArgs &o, const float *q, const float *k_cache, const float *v_cache, uint8_t *img,
-                        int n, int pos, int H, int KV, int C, cudaStream_t s);
+                        int n, int pos, const int32_t *d_pos, int H, int KV, int C, cudaStream_t s);
 int launch_rope(float *q, float *k, const float *c, const float *sn, int pos, int H, int KV, int hd, cudaStream_t s);
 int launch_kv_store(float *kc, float *vc, const float *k, const float *v, int pos, int KV, int C, int hd,
                     cudaStream_t s);

@@ -124,13 +124,15 @@ struct PfArgs {
     const float *k_cache, *v_cache;  // fp32 [KV, C, 128]
     const float *q;                  // fp32 [n, H * 128], after RoPE
     uint8_t *img;                    // [KV][ntk][PF_TILE]
-    int C, ntk, rows;                // capacity, image tiles per head, rows converted (pos + n)
+    int C, ntk;                      // capacity, image tiles per head
     int n, pos, H, KV, G, GP, TPT;   // TPT = 128 / GP tokens per query tile
+    const int32_t *d_pos;            // the chunk's first position on the device (or null: pos)
     float scale_log2;                // log2(e) / sqrt(128)
     AttnArgs o;                      // outputs (out, out_q8, out_img, out_pack, img_groups, H, status)
 };
 
-// Key tile t of KV head g into the image; rows from `rows` on are zeros.
+// Key tile t of KV head g into the image; rows from pos + n on are zeros.
+// A chunk outside the cache converts nothing.
 __global__ void __launch_bounds__(256) k_pf_kv_image(const PfArgs a) {
     const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
     uint8_t *dst = a.img + (static_cast<size_t>(g) * a.ntk + t) * PF_TILE;
@@ -138,9 +140,13 @@ __global__ void __launch_bounds__(256) k_pf_kv_image(const PfArgs a) {
     const float *vc = a.v_cache + static_cast<size_t>(g) * a.C * PF_HD;
     pdl_trigger();
     pdl_wait();  // the chunk's rows were stored by the projection grid
-    {            // K: thread -> row tid / 4, dims 32 (tid % 4) ..
+    const int pos = a.d_pos ? *a.d_pos : a.pos;
+    if (pos < 0 || pos > a.C - a.n) return;
+    const int rows = pos + a.n;
+    if (t * PF_N >= rows) return;  // a tile past the chunk (grid sized by the capacity)
+    {                              // K: thread -> row tid / 4, dims 32 (tid % 4) ..
         const int r = tid >> 2, d0 = (tid & 3) * 32, row = t * PF_N + r;
-        const bool in = row < a.rows;
+        const bool in = row < rows;
         const float4 *src = reinterpret_cast<const float4 *>(kc + static_cast<size_t>(in ? row : 0) * PF_HD + d0);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -164,7 +170,7 @@ __global__ void __launch_bounds__(256) k_pf_kv_image(const PfArgs a) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int row = t * PF_N + c0 + 8 * cc + i;
-                x[i] = row < a.rows ? vc[static_cast<size_t>(row) * PF_HD + d] : 0.0f;
+                x[i] = row < rows ? vc[static_cast<size_t>(row) * PF_HD + d] : 0.0f;
             }
             uint4 hi, lo;
             bf_split8(x, hi, lo);
@@ -186,7 +192,15 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
     const int g = blockIdx.y;
     const int tl0 = blockIdx.x * a.TPT;                  // the tile's first token
     const int tl_last = min(a.n - 1, tl0 + a.TPT - 1);  // and its last
-    const int nkt = (a.pos + tl_last + 1 + PF_N - 1) / PF_N;
+    // the chunk's position (a device position was set before the chunk's
+    // first kernel, which every later one follows)
+    const int pos = a.d_pos ? *a.d_pos : a.pos;
+    if (pos < 0 || pos > a.C - a.n) {  // a chunk outside the cache: nothing attended, nothing written
+        pdl_trigger();
+        pdl_wait();
+        return;
+    }
+    const int nkt = (pos + tl_last + 1 + PF_N - 1) / PF_N;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < PF_NST; ++i) {
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
         const int r = threadIdx.x;
         const int tl = tl0 + r / a.GP, hs = r % a.GP;
         const bool valid = tl < a.n && hs < a.G;
-        const int limit = a.pos + min(tl, a.n - 1);  // the last key row this row sees
+        const int limit = pos + min(tl, a.n - 1);  // the last key row this row sees
         const uint32_t lanes = taddr + (static_cast<uint32_t>(warp * 32) << 16);
         {  // the row's q as bf16 hi / lo into its TMEM lane (the A operand of S)
             const float4 *qr = reinterpret_cast<const float4 *>(
@@ -271,7 +285,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) k_pf_attn(const PfArgs a) {
             const int k0 = j * PF_N;
             // the causal mask only where a row of this tile may end inside the
             // key tile (the same for the whole CTA: its first token's limit)
-            if (k0 + PF_N - 1 > a.pos + tl0) {
+            if (k0 + PF_N - 1 > pos + tl0) {
 #pragma unroll
                 for (int c = 0; c < PF_N; ++c)
                     if (k0 + c > limit) p[c] = -INFINITY;
@@ -454,7 +468,7 @@ size_t prefill_img_bytes(int KV, int C) {
 }
 
 int launch_prefill_attn(const AttnArgs &o, const float *q, const float *k_cache, const float *v_cache, uint8_t *img,
-                        int n, int pos, int H, int KV, int C, cudaStream_t s) {
+                        int n, int pos, const int32_t *d_pos, int H, int KV, int C, cudaStream_t s) {
     PfArgs a{};
     a.k_cache = k_cache;
     a.v_cache = v_cache;
@@ -462,9 +476,9 @@ int launch_prefill_attn(const AttnArgs &o, const float *q, const float *k_cache,
     a.img = img;
     a.C = C;
     a.ntk = (C + PF_N - 1) / PF_N;
-    a.rows = pos + n;
     a.n = n;
     a.pos = pos;
+    a.d_pos = d_pos;
     a.H = H;
     a.KV = KV;
     a.G = H / KV;
@@ -475,8 +489,10 @@ int launch_prefill_attn(const AttnArgs &o, const float *q, const float *k_cache,
     a.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(PF_HD));
     a.o = o;
     void *args[] = {&a};
-    cudaError_t e = launch(reinterpret_cast<const void *>(k_pf_kv_image), dim3((a.rows + PF_N - 1) / PF_N, KV),
-                           dim3(256), 0, s, true, args);
+    // the image's tiles: those of the chunk's rows, or every tile of the
+    // capacity when the position is read on the device
+    const int tiles = d_pos ? a.ntk : (pos + n + PF_N - 1) / PF_N;
+    cudaError_t e = launch(reinterpret_cast<const void *>(k_pf_kv_image), dim3(tiles, KV), dim3(256), 0, s, true, args);
     if (e != cudaSuccess) return -5;
     const void *fn = reinterpret_cast<const void *>(k_pf_attn);
     ensure_smem(fn, PF_SMEM);

@@ -296,3 +296,99 @@ def test_attn_prefill_argument_errors(dev):
     assert f(bytes_=nb - 257) == q.CK_ESCRATCH
     assert q.ck_attn_prefill_scratch_size(H, KV, 64, C) == 0
     ok(f(pos=56))
+
+
+def _devpos_call(c, pos_t, x=None, out=None):
+    g, w = c.g, c.w
+    x = g["x"] if x is None else x
+    return q.ck_prefill_layer_devpos(c.out if out is None else out, x, x, g["wq"], g["wk"], g["wv"], g["wo"],
+                                     g["gamma"], g["bq"], g["bk"], g["bv"], g["bo"], c.kc, c.vc, g["cos"], g["sin"],
+                                     pos_t, c.n, w.D, w.H, w.KV, w.hd, w.capacity, w.eps, c.scratch, c.nbytes)
+
+
+@pytest.mark.parametrize("shape", ["7b", "tiny"])
+def test_prefill_devpos_equals_host_position(dev, shape):
+    """The position read on the device gives the same bits as the host
+    position (tensor-core attention at head_dim 128, decode path at 64)."""
+    if shape == "7b":
+        w, pos, n = dataclasses.replace(synth.WORKLOADS["7b8k"], capacity=1024), 300, 20
+    else:
+        w, pos, n = synth.WORKLOADS["tiny"], 16, 9
+    c = Chunk(dev, w, pos, n, seed=101)
+    ok(c.call())
+    ref_out, ref_k, ref_v = H(c.out).copy(), H(c.kc).copy(), H(c.vc).copy()
+    c.kc.copy_(T(c.kc0, dev))
+    c.vc.copy_(T(c.vc0, dev))
+    c.out.fill_(0.0)
+    ok(_devpos_call(c, torch.tensor([pos], dtype=torch.int32, device=dev)))
+    assert np.array_equal(H(c.out), ref_out)
+    assert np.array_equal(H(c.kc), ref_k, equal_nan=True) and np.array_equal(H(c.vc), ref_v, equal_nan=True)
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == 0
+
+
+@pytest.mark.parametrize("shape", ["7b", "tiny"])
+def test_prefill_devpos_out_of_range_writes_nothing(dev, shape):
+    if shape == "7b":
+        w, n = dataclasses.replace(synth.WORKLOADS["7b8k"], capacity=256), 16
+    else:
+        w, n = synth.WORKLOADS["tiny"], 5
+    c = Chunk(dev, w, 10, n, seed=102)
+    c.out.fill_(7.0)
+    q.ck_device_status()  # clear
+    ok(_devpos_call(c, torch.tensor([w.capacity - n + 1], dtype=torch.int32, device=dev)))
+    assert np.all(H(c.out) == 7.0)
+    assert np.array_equal(H(c.kc), c.kc0, equal_nan=True) and np.array_equal(H(c.vc), c.vc0, equal_nan=True)
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == q.CK_ERANGE
+    assert _devpos_call(c, None) == q.CK_EINVAL
+
+
+def test_prefill_devpos_graph_replay_moves_the_chunk(dev):
+    """One captured graph prefills two consecutive chunks of 8 tokens (the
+    position advanced on the device between replays); the result equals two
+    host-position calls."""
+    w = dataclasses.replace(synth.WORKLOADS["7b8k"], capacity=512)
+    n, p0 = 8, 200
+    c = Chunk(dev, w, p0, 2 * n, seed=103)  # 16 tokens of input, two chunks of 8
+    nb = q.ck_prefill_layer_scratch_size(n, w.D, w.H, w.KV, w.hd, w.capacity)
+    g = c.g
+    # reference: two host-position calls
+    sc = torch.empty(nb, dtype=torch.uint8, device=dev)
+    ref = []
+    for k in range(2):
+        xs = g["x"][k * n:(k + 1) * n].contiguous()
+        o = torch.empty((n, w.D), dtype=torch.float32, device=dev)
+        ok(q.ck_prefill_layer(o, xs, xs, g["wq"], g["wk"], g["wv"], g["wo"], g["gamma"], g["bq"], g["bk"], g["bv"],
+                              g["bo"], c.kc, c.vc, g["cos"], g["sin"], p0 + k * n, n, w.D, w.H, w.KV, w.hd,
+                              w.capacity, w.eps, sc, nb))
+        ref.append(H(o).copy())
+    ref_k, ref_v = H(c.kc).copy(), H(c.vc).copy()
+    # the graph
+    c.kc.copy_(T(c.kc0, dev))
+    c.vc.copy_(T(c.vc0, dev))
+    xin = torch.empty((n, w.D), dtype=torch.float32, device=dev)
+    oo = torch.empty((n, w.D), dtype=torch.float32, device=dev)
+    dpos = torch.tensor([p0], dtype=torch.int32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    xin.copy_(g["x"][:n])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        rc = q.ck_prefill_layer_devpos(oo, xin, xin, g["wq"], g["wk"], g["wv"], g["wo"], g["gamma"], g["bq"], g["bk"],
+                                       g["bv"], g["bo"], c.kc, c.vc, g["cos"], g["sin"], dpos, n, w.D, w.H, w.KV,
+                                       w.hd, w.capacity, w.eps, sc, nb, st.cuda_stream)
+    ok(rc)
+    got = []
+    for k in range(2):
+        xin.copy_(g["x"][k * n:(k + 1) * n])
+        dpos.fill_(p0 + k * n)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got.append(H(oo).copy())
+    for k in range(2):
+        assert np.array_equal(got[k], ref[k]), k
+    assert np.array_equal(H(c.kc), ref_k, equal_nan=True) and np.array_equal(H(c.vc), ref_v, equal_nan=True)
+    rc, st2 = q.ck_device_status()
+    assert rc == 0 and st2 == 0
