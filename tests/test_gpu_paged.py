@@ -147,3 +147,35 @@ def test_paged_rejects_bad_arguments(dev):
     assert call(args(kind=1, hd=96, H=6, KV=2)) == q.CK_EINVAL
     assert call(args(kind=2, ks=0.0)) == q.CK_EINVAL
     assert call(args(nbytes=16)) == q.CK_ESCRATCH
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_paged_tensor_core_kernel_flags_bad_entries(dev, kind):
+    """The same checks on the head_dim 128 bf16 / fp8 kernel (scores and P.V on
+    the tensor cores): an entry outside the pool is flagged and the other
+    sequence stays exact; a length past the table is flagged and gives zeros."""
+    rng = np.random.default_rng(90 + kind)
+    B, Hq, KV, hd, bs, maxb = 2, 28, 4, 128, 64, 4
+    nblk = 8
+    kp, vp, ks, vs = make_pools(rng, kind, nblk, KV, bs, hd)
+    tables = np.array([[0, 1, 2, 3], [4, 5, 1000, 7]], np.int32)
+    lens = np.array([200, 230], np.int32)
+    qv = rng.standard_normal(B * Hq * hd).astype(np.float32)
+    nbytes = q.ck_attn_paged_scratch_size(B, Hq, KV, hd, bs, maxb, 0)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty(B * Hq * hd, dtype=torch.float32, device=dev)
+    q.ck_device_status()
+    assert q.ck_attn_decode_gqa_paged(T(qv, dev), T(kp, dev), T(vp, dev), out, T(tables, dev), T(lens, dev), B, Hq,
+                                      KV, hd, bs, maxb, nblk, 0, kind, ks, vs, scratch, nbytes) == q.CK_OK
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == q.CK_ERANGE
+    ref0 = oracle.attention_paged(qv[:Hq * hd], kp, vp, tables[:1], lens[:1], 1, Hq, KV, hd, bs, maxb, 0, kind, ks,
+                                  vs)
+    assert_close(H(out)[:Hq * hd], ref0, "sequence 0")
+    lens2 = np.array([200, maxb * bs + 1], np.int32)
+    assert q.ck_attn_decode_gqa_paged(T(qv, dev), T(kp, dev), T(vp, dev), out, T(tables[:, :4] % nblk, dev),
+                                      T(lens2, dev), B, Hq, KV, hd, bs, maxb, nblk, 0, kind, ks, vs, scratch,
+                                      nbytes) == q.CK_OK
+    rc, st = q.ck_device_status()
+    assert rc == 0 and st == q.CK_ERANGE
+    assert np.all(H(out)[Hq * hd:] == 0.0)
