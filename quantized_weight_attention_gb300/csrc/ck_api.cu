@@ -454,7 +454,15 @@ int ck_attn_decode_gqa_paged(const float *q, const void *k_pool, const void *v_p
     if (!scratch) return CK_ESCRATCH;
     if (!aligned16(scratch)) return CK_EALIGN;
     const int rows = paged_rows(block_size, max_blocks_per_seq, sliding_window);
-    const int S = attn_splits_batched(batch, num_kv_heads, rows);
+    int S = attn_splits_batched(batch, num_kv_heads, rows);
+    // the tensor-core kernel pays more per CTA (TMEM, q image, the first
+    // tiles) and overlaps two tiles per CTA: about 4 CTAs per SM instead of 8
+    // (fewer splits fit the scratch sized for more)
+    const int nsm = device_info().num_sms;
+    if (attention_tc_ok(kv_dtype, num_heads, num_kv_heads, head_dim) && 2 * batch * num_kv_heads > nsm) {
+        const int s4 = (4 * nsm + batch * num_kv_heads - 1) / (batch * num_kv_heads);
+        if (s4 < S) S = s4 < 1 ? 1 : s4;
+    }
     if (scratch_bytes < attn_part_bytes(batch, num_heads, num_kv_heads, head_dim, S)) return CK_ESCRATCH;
     unsigned *st = status_word();
     if (!st) return CK_ECUDA;
